@@ -1,0 +1,213 @@
+/* moe_oracle.c -- TEST INFRASTRUCTURE ONLY: plain fp64 reference of one MoE FFN layer.
+ * The definitions and their sources are listed in moe_oracle.h.  No blocking, no fusion, no
+ * reordering: each function is the textbook loop of the step it names. */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+double oracle_elem(const void* base, int dtype, size_t i) {
+  if (dtype == ORACLE_BF16) {
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  return (double)((const float*)base)[i];
+}
+
+/* Linear gate followed by the score function.  Page "Expert-Parallel MoE Inference",
+ * section "Deeper Analysis": a tiny linear gate scores every expert for every token and a
+ * softmax is applied.  Sigmoid scoring with a selection-only bias is the alternative the
+ * layer specification adds for the DeepSeek-V3-shaped workloads. */
+int oracle_router_scores(int n_tok, int d, int E, int dtype, const void* x_rows,
+                         const void* w_router, int score_fn, const float* bias,
+                         double* logits, double* score, double* key) {
+  if (n_tok < 0 || d < 1 || E < 1 || !x_rows || !w_router) return -1;
+  if (score_fn != ORACLE_SOFTMAX && score_fn != ORACLE_SIGMOID) return -1;
+  double* l = (double*)malloc(sizeof(double) * (size_t)E);
+  double* s = (double*)malloc(sizeof(double) * (size_t)E);
+  if (!l || !s) { free(l); free(s); return -1; }
+  for (int t = 0; t < n_tok; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i)
+        acc += oracle_elem(x_rows, dtype, (size_t)t * d + i) *
+               oracle_elem(w_router, dtype, (size_t)e * d + i);
+      l[e] = acc;
+    }
+    if (score_fn == ORACLE_SOFTMAX) {
+      double mx = l[0];
+      for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
+      double den = 0.0;
+      for (int e = 0; e < E; ++e) den += exp(l[e] - mx);
+      for (int e = 0; e < E; ++e) s[e] = exp(l[e] - mx) / den;
+    } else {
+      for (int e = 0; e < E; ++e) s[e] = 1.0 / (1.0 + exp(-l[e]));
+    }
+    for (int e = 0; e < E; ++e) {
+      size_t o = (size_t)t * E + e;
+      if (logits) logits[o] = l[e];
+      if (score) score[o] = s[e];
+      if (key) {
+        if (score_fn == ORACLE_SOFTMAX) key[o] = l[e];  /* softmax is monotone in the logit */
+        else key[o] = s[e] + (bias ? (double)bias[e] : 0.0);
+      }
+    }
+  }
+  free(l);
+  free(s);
+  return 0;
+}
+
+/* Keep the top-k experts (page "Expert-Parallel MoE Inference", "Deeper Analysis"), then
+ * renormalise the kept scores to sum to one.  Selection: k times, take the unselected expert
+ * with the largest key; among equal keys the lower id. */
+int oracle_topk(int n_tok, int E, int k, const double* key, const double* score,
+                int* topk_idx, double* topk_w, double* margin) {
+  if (n_tok < 0 || E < 1 || k < 1 || k > E || !key || !topk_idx) return -1;
+  if (topk_w && !score) return -1;
+  char* taken = (char*)malloc((size_t)E);
+  if (!taken) return -1;
+  for (int t = 0; t < n_tok; ++t) {
+    const double* kr = key + (size_t)t * E;
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || kr[e] > kr[best]) best = e;  /* strict: equal keys keep the lower id */
+      }
+      taken[best] = 1;
+      topk_idx[(size_t)t * k + j] = best;
+    }
+    if (margin) {
+      int next = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (next < 0 || kr[e] > kr[next])) next = e;
+      margin[t] = next < 0 ? INFINITY : kr[topk_idx[(size_t)t * k + k - 1]] - kr[next];
+    }
+    if (topk_w) {
+      const double* sr = score + (size_t)t * E;
+      double den = 0.0;
+      for (int j = 0; j < k; ++j) den += sr[topk_idx[(size_t)t * k + j]];
+      for (int j = 0; j < k; ++j) topk_w[(size_t)t * k + j] = sr[topk_idx[(size_t)t * k + j]] / den;
+    }
+  }
+  free(taken);
+  return 0;
+}
+
+/* Group the (token, slot) assignments by expert, token order preserved within an expert:
+ * the single-GPU form of the dispatch all-to-all (page "Expert-Parallel MoE Inference",
+ * "The all-to-all dispatch and combine, step by step"; page "MoE Expert Parallelism in
+ * Practice", "Core Principles" part 1, "dispatch tokens to selected experts"). */
+int oracle_dispatch(int T, int E, int k, const int* topk_idx, int* counts, int* offsets,
+                    int* sorted_token, int* slot_pos) {
+  if (T < 0 || E < 1 || k < 1 || !topk_idx || !counts || !offsets) return -1;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (size_t i = 0; i < (size_t)T * k; ++i) {
+    int e = topk_idx[i];
+    if (e < 0 || e >= E) return -1;
+    counts[e] += 1;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  if (sorted_token || slot_pos) {
+    int p = 0;
+    for (int e = 0; e < E; ++e)
+      for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j)
+          if (topk_idx[(size_t)t * k + j] == e) {
+            if (sorted_token) sorted_token[p] = t;
+            if (slot_pos) slot_pos[(size_t)t * k + j] = p;
+            ++p;
+          }
+  }
+  return 0;
+}
+
+int oracle_gather(int R, int d, const int* sorted_token, const double* x, double* xs) {
+  if (R < 0 || d < 1 || !sorted_token || !x || !xs) return -1;
+  for (int p = 0; p < R; ++p)
+    for (int c = 0; c < d; ++c) xs[(size_t)p * d + c] = x[(size_t)sorted_token[p] * d + c];
+  return 0;
+}
+
+/* Weighted sum of the k expert outputs back in token order (page "Expert-Parallel MoE
+ * Inference", "Deeper Analysis"; page "MoE Expert Parallelism in Practice", "Core
+ * Principles" part 1, combine and map back to the original token order). */
+int oracle_combine(int T, int k, int d, const int* slot_pos, const double* topk_w,
+                   const double* ys, const double* y_shared, double* out) {
+  if (T < 0 || k < 1 || d < 1 || !slot_pos || !topk_w || !ys || !out) return -1;
+  for (int t = 0; t < T; ++t)
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int j = 0; j < k; ++j)
+        acc += topk_w[(size_t)t * k + j] * ys[(size_t)slot_pos[(size_t)t * k + j] * d + c];
+      if (y_shared) acc += y_shared[(size_t)t * d + c];
+      out[(size_t)t * d + c] = acc;
+    }
+  return 0;
+}
+
+/* One expert: SwiGLU feed-forward block. */
+int oracle_swiglu_ffn(int d, int F, int dtype, const double* xrow, const void* w_gate_up,
+                      const void* w_down, double* y) {
+  if (d < 1 || F < 1 || !xrow || !w_gate_up || !w_down || !y) return -1;
+  double* h = (double*)malloc(sizeof(double) * (size_t)F);
+  if (!h) return -1;
+  for (int f = 0; f < F; ++f) {
+    double g = 0.0, u = 0.0;
+    for (int i = 0; i < d; ++i) {
+      g += xrow[i] * oracle_elem(w_gate_up, dtype, (size_t)f * d + i);
+      u += xrow[i] * oracle_elem(w_gate_up, dtype, (size_t)(F + f) * d + i);
+    }
+    h[f] = g / (1.0 + exp(-g)) * u;
+  }
+  for (int c = 0; c < d; ++c) {
+    double acc = 0.0;
+    for (int f = 0; f < F; ++f) acc += h[f] * oracle_elem(w_down, dtype, (size_t)c * F + f);
+    y[c] = acc;
+  }
+  free(h);
+  return 0;
+}
+
+/* out[t] = sum_j w_tj FFN_{S_tj}(x_t) + FFN_shared(x_t), shared expert with weight 1
+ * (page "Tensor vs Expert vs Data Parallelism for MoE Serving", "Context and Background":
+ * routed experts plus a shared expert). */
+int oracle_layer_rows(const oracle_layer* L, int n_tok, const void* x_rows, const int* topk_idx,
+                      const double* topk_w, double* out) {
+  if (!L || n_tok < 0 || !x_rows || !topk_idx || !topk_w || !out) return -1;
+  if (L->d < 1 || L->E < 1 || L->k < 1 || L->k > L->E || L->F < 1 || L->Fs < 0) return -1;
+  if (!L->w_gate_up || !L->w_down) return -1;
+  if (L->Fs > 0 && (!L->sh_gate_up || !L->sh_down)) return -1;
+  const int d = L->d;
+  double* xr = (double*)malloc(sizeof(double) * (size_t)d);
+  double* y = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!xr || !y) { free(xr); free(y); return -1; }
+  int rc = 0;
+  for (int t = 0; t < n_tok && rc == 0; ++t) {
+    for (int i = 0; i < d; ++i) xr[i] = oracle_elem(x_rows, L->dtype, (size_t)t * d + i);
+    double* o = out + (size_t)t * d;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int j = 0; j < L->k; ++j) {
+      int e = topk_idx[(size_t)t * L->k + j];
+      if (e < 0 || e >= L->E) { rc = -1; break; }
+      if (!L->w_gate_up[e] || !L->w_down[e]) { rc = -2; break; }
+      oracle_swiglu_ffn(d, L->F, L->dtype, xr, L->w_gate_up[e], L->w_down[e], y);
+      double w = topk_w[(size_t)t * L->k + j];
+      for (int c = 0; c < d; ++c) o[c] += w * y[c];
+    }
+    if (rc == 0 && L->Fs > 0) {
+      oracle_swiglu_ffn(d, L->Fs, L->dtype, xr, L->sh_gate_up, L->sh_down, y);
+      for (int c = 0; c < d; ++c) o[c] += y[c];
+    }
+  }
+  free(xr);
+  free(y);
+  return rc;
+}

@@ -1,0 +1,288 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+Each test names the mistake it is built to catch.  Sources of the definitions are in
+oracle/moe_oracle.h.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit, softmax
+
+import oracle
+from moe_inputs import host
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def silu(g):
+    return g * expit(g)
+
+
+def f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+# ------------------------------------------------------------------ element decoding
+def test_bf16_element_decoding():
+    bits = np.array([0x3F80, 0xC000, 0x3F00, 0x4049, 0x0000, 0x8000], dtype=np.uint16)
+    want = [1.0, -2.0, 0.5, 3.140625, 0.0, -0.0]
+    got = [oracle.lib().oracle_elem(bits.ctypes.data, oracle.BF16, i) for i in range(6)]
+    assert got == want
+
+
+# ------------------------------------------------------------------ hand-worked cases
+def test_hand_case_softmax_router_and_swiglu():
+    """d=2, E=4, k=2, F=1, x=[1,0], logits [2,1,0,-1].  Closed forms: S=(0,1),
+    w0 = 1/(1+e^-1), w1 = 1/(1+e^1); expert e has gate weight a_e=e+1, up 1, down [1,0],
+    so out = [w0*silu(1) + w1*silu(2), 0].  Catches: wrong softmax direction, missing
+    renormalisation, gate/up swapped, wrong output row of W_down."""
+    x = f32([[1, 0]])
+    wr = f32([[2, 0], [1, 0], [0, 0], [-1, 0]])
+    _, s, key = oracle.router_scores(x, wr, oracle.SOFTMAX)
+    idx, w, margin = oracle.topk(key, s, 2)
+    assert idx.tolist() == [[0, 1]]
+    assert w[0, 0] == pytest.approx(1 / (1 + math.exp(-1)), abs=1e-15)
+    assert w[0, 1] == pytest.approx(1 / (1 + math.exp(1)), abs=1e-15)
+    assert margin[0] == pytest.approx(1.0)
+    gu = {e: f32([[e + 1, 0], [1, 0]]) for e in range(4)}     # [2F][d]: gate row, up row
+    dn = {e: f32([[1], [0]]) for e in range(4)}               # [d][F]
+    out = oracle.layer_rows(x, idx, w, gu, dn)
+    s1 = 1 / (1 + math.exp(-1))
+    s2 = 2 / (1 + math.exp(-2))
+    want = (1 / (1 + math.exp(-1))) * s1 + (1 / (1 + math.exp(1))) * s2
+    assert out[0, 0] == pytest.approx(want, abs=1e-14)
+    assert out[0, 0] == pytest.approx(1.0082122816, abs=1e-9)
+    assert out[0, 1] == 0.0
+
+
+def test_hand_case_tie_break_lower_id():
+    """logits [1,1,1,0], k=2 -> S=(0,1), w=(1/2,1/2).  Catches a tie-break toward the
+    higher id or an unstable selection."""
+    x = f32([[1, 0]])
+    wr = f32([[1, 0], [1, 0], [1, 0], [0, 0]])
+    _, s, key = oracle.router_scores(x, wr, oracle.SOFTMAX)
+    idx, w, margin = oracle.topk(key, s, 2)
+    assert idx.tolist() == [[0, 1]]
+    assert w.tolist() == [[0.5, 0.5]]
+    assert margin[0] == 0.0
+
+
+def test_hand_case_sigmoid_bias_selects_but_does_not_weight():
+    """l=[0,.5,-.5,1], b=[0,-.6,.7,0]: keys sigma+b = [.5, .0225, 1.0775, .7311] -> S=(2,3);
+    w from the UNBIASED sigma: sigma(-.5)/(sigma(-.5)+sigma(1)).  Catches weights taken
+    from biased keys, bias ignored in selection, or a sign error in the sigmoid."""
+    x = f32([[1, 0]])
+    wr = f32([[0, 0], [0.5, 0], [-0.5, 0], [1, 0]])
+    bias = f32([0, -0.6, 0.7, 0])
+    _, s, key = oracle.router_scores(x, wr, oracle.SIGMOID, bias)
+    idx, w, _ = oracle.topk(key, s, 2)
+    assert idx.tolist() == [[2, 3]]
+    sa, sb = 1 / (1 + math.exp(0.5)), 1 / (1 + math.exp(-1.0))
+    assert w[0, 0] == pytest.approx(sa / (sa + sb), abs=1e-15)
+    assert w[0, 0] == pytest.approx(0.3405564903, abs=1e-9)
+    assert key[0, 1] == pytest.approx(1 / (1 + math.exp(-0.5)) + float(np.float32(-0.6)), abs=1e-15)
+
+
+# ------------------------------------------------------------------ library / closed-form reductions
+def test_logits_equal_library_matmul_and_softmax():
+    """Logits = x W_r^T (numpy matmul), scores = scipy softmax / expit.  Non-square shapes
+    catch a transposed operand; any dropped term changes the matmul."""
+    rng = np.random.default_rng(1)
+    x = f32(rng.standard_normal((7, 24)))
+    wr = f32(rng.standard_normal((5, 24)) / 5)
+    bias = f32(rng.uniform(-0.1, 0.1, 5))
+    ref = x.astype(np.float64) @ wr.astype(np.float64).T
+    lg, s, key = oracle.router_scores(x, wr, oracle.SOFTMAX)
+    np.testing.assert_allclose(lg, ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(s, softmax(ref, axis=1), rtol=1e-13)
+    np.testing.assert_array_equal(key, lg)
+    lg2, s2, key2 = oracle.router_scores(x, wr, oracle.SIGMOID, bias)
+    np.testing.assert_allclose(s2, expit(ref), rtol=1e-13)
+    np.testing.assert_allclose(key2, expit(ref) + bias.astype(np.float64), rtol=1e-13)
+
+
+def test_softmax_renorm_closed_form():
+    """After renormalisation over the selected set, w_j = 1 / (1 + sum_{j' != j} e^(l_j' - l_j))."""
+    rng = np.random.default_rng(2)
+    l = rng.standard_normal((20, 16)) * 2
+    s = softmax(l, axis=1)
+    idx, w, _ = oracle.topk(l, s, 4)
+    for t in range(20):
+        sel = l[t, idx[t]]
+        for j in range(4):
+            want = 1.0 / (1.0 + sum(math.exp(sel[jj] - sel[j]) for jj in range(4) if jj != j))
+            assert w[t, j] == pytest.approx(want, rel=1e-13)
+    np.testing.assert_allclose(w.sum(1), 1.0, atol=1e-15)
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (5, 2), (6, 3), (8, 4), (10, 3), (10, 10), (9, 8)])
+def test_topk_brute_force_with_ties(E, k):
+    """Against brute force over all C(E,k) subsets: the selected set is the unique subset
+    whose every member beats every non-member (larger key, or equal key and lower id).
+    Keys are quantised so ties are frequent.  Order: key descending, ties lower id."""
+    rng = np.random.default_rng(E * 31 + k)
+    key = np.round(rng.standard_normal((200, E)) * 2) / 2
+    score = rng.uniform(0.1, 1.0, (200, E))
+    idx, w, margin = oracle.topk(key, score, k)
+
+    def beats(a, b, kr):
+        return kr[a] > kr[b] or (kr[a] == kr[b] and a < b)
+
+    for t in range(200):
+        kr = key[t]
+        valid = [S for S in itertools.combinations(range(E), k)
+                 if all(beats(a, b, kr) for a in S for b in range(E) if b not in S)]
+        assert len(valid) == 1
+        assert sorted(idx[t].tolist()) == list(valid[0])
+        order = sorted(valid[0], key=lambda e: (-kr[e], e))
+        assert idx[t].tolist() == order
+        sel = score[t, order]
+        np.testing.assert_allclose(w[t], sel / sel.sum(), rtol=1e-15)
+        if k < E:
+            rest = max(kr[b] for b in range(E) if b not in valid[0])
+            assert margin[t] == kr[order[-1]] - rest
+        else:
+            assert margin[t] == np.inf
+
+
+# ------------------------------------------------------------------ dispatch tables
+def _random_routing(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (37, 8, 2), (100, 16, 5), (64, 64, 64)])
+def test_dispatch_against_stable_sort_and_invariants(T, E, k):
+    """Against Python's stable sort of (expert, token) pairs; invariants: sum counts = T*k,
+    offsets = exclusive scan, segments ascending in t, slot_pos o sorted_token = identity."""
+    idx = _random_routing(T, E, k, T + E + k)
+    counts, offsets, st, sp = oracle.dispatch(idx, E)
+    pairs = sorted(((int(idx[t, j]), t, j) for t in range(T) for j in range(k)))
+    assert st.tolist() == [t for _, t, _ in pairs]
+    for p, (_, t, j) in enumerate(pairs):
+        assert sp[t, j] == p
+    assert counts.sum() == T * k
+    np.testing.assert_array_equal(np.bincount(idx.ravel(), minlength=E), counts)
+    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+    for e in range(E):
+        seg = st[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)
+    for t in range(T):
+        for j in range(k):
+            assert st[sp[t, j]] == t
+
+
+def test_dispatch_reproduces_capacity_worked_example():
+    """Page worked example: 512 decode tokens, top-8 of 256 experts, EP=16 -> 4096
+    assignments, 16 per expert under perfectly even routing, 256 per 16-expert GPU."""
+    g = json.load(open(os.path.join(GOLDEN, "capacity_worked_example.json")))
+    T, E, k, ep = g["tokens"], g["n_experts"], g["top_k"], g["ep_size"]
+    idx = np.array([[(8 * t + j) % E for j in range(k)] for t in range(T)], dtype=np.int32)
+    counts, offsets, _, _ = oracle.dispatch(idx, E)
+    assert offsets[-1] == g["expected"]["assignments"]
+    assert set(counts.tolist()) == {g["expected"]["tokens_per_expert_uniform"]}
+    per_gpu = counts.reshape(ep, E // ep).sum(1)
+    assert set(per_gpu.tolist()) == {g["expected"]["token_experts_per_gpu_uniform"]}
+    skew = g["expected"]["busiest_gpu_skew"]
+    assert round(skew * per_gpu.mean()) == g["expected"]["busiest_gpu_token_experts_approx"]
+
+
+def test_identity_experts_round_trip_returns_x():
+    """Dispatch (gather) then combine with identity experts returns x (weights sum to 1)."""
+    rng = np.random.default_rng(5)
+    T, E, k, d = 50, 12, 3, 9
+    x = rng.standard_normal((T, d))
+    l = rng.standard_normal((T, E))
+    idx, w, _ = oracle.topk(l, softmax(l, axis=1), k)
+    _, _, st, sp = oracle.dispatch(idx, E)
+    xs = oracle.gather(st, x)
+    out = oracle.combine(sp, w, xs)
+    np.testing.assert_allclose(out, x, atol=1e-12)
+    shared = rng.standard_normal((T, d))
+    np.testing.assert_allclose(oracle.combine(sp, w, xs, shared), x + shared, atol=1e-12)
+
+
+def test_combine_against_einsum():
+    rng = np.random.default_rng(6)
+    T, k, d, R = 11, 3, 5, 40
+    sp = rng.integers(0, R, (T, k)).astype(np.int32)
+    w = rng.uniform(0, 1, (T, k))
+    ys = rng.standard_normal((R, d))
+    np.testing.assert_allclose(oracle.combine(sp, w, ys), np.einsum("tj,tjc->tc", w, ys[sp]),
+                               rtol=1e-14, atol=1e-14)
+
+
+# ------------------------------------------------------------------ expert FFN
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_swiglu_against_library_matmul(dtype):
+    """y = W_d (silu(W_g x) * (W_u x)) with numpy matmul and scipy expit; F != d catches a
+    transposed weight, the asymmetric silu catches gate/up swapped."""
+    rng = np.random.default_rng(7)
+    d, F = 12, 20
+    wgu = f32(rng.standard_normal((2 * F, d)) / math.sqrt(d))
+    wd = f32(rng.standard_normal((d, F)) / math.sqrt(F))
+    x = rng.standard_normal(d)
+    if dtype == "bf16":
+        wgu_s, wd_s = host.f32_to_bf16_bits(wgu), host.f32_to_bf16_bits(wd)
+        wgu = host.bf16_bits_to_f32(wgu_s); wd = host.bf16_bits_to_f32(wd_s)
+    else:
+        wgu_s, wd_s = wgu, wd
+    g = wgu[:F].astype(np.float64) @ x
+    u = wgu[F:].astype(np.float64) @ x
+    want = wd.astype(np.float64) @ (silu(g) * u)
+    np.testing.assert_allclose(oracle.swiglu_ffn(x, wgu_s, wd_s), want, rtol=1e-12, atol=1e-13)
+
+
+def test_single_expert_layer_is_dense_swiglu():
+    """E = k = 1: the layer is one dense SwiGLU FFN (weight 1)."""
+    rng = np.random.default_rng(8)
+    T, d, F = 6, 16, 24
+    x = f32(rng.standard_normal((T, d)))
+    wr = f32(rng.standard_normal((1, d)))
+    wgu = f32(rng.standard_normal((1, 2 * F, d)) / 4)
+    wd = f32(rng.standard_normal((1, d, F)) / 5)
+    _, s, key = oracle.router_scores(x, wr, oracle.SOFTMAX)
+    idx, w, _ = oracle.topk(key, s, 1)
+    assert np.all(idx == 0) and np.all(w == 1.0)
+    out = oracle.layer_rows(x, idx, w, wgu, wd)
+    xd = x.astype(np.float64)
+    want = (silu(xd @ wgu[0, :F].T.astype(np.float64)) * (xd @ wgu[0, F:].T.astype(np.float64))) \
+        @ wd[0].T.astype(np.float64)
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-13)
+
+
+def test_identical_experts_make_output_routing_independent():
+    """All experts equal -> out = dense FFN regardless of routing (weights sum to 1);
+    the shared expert adds its own dense FFN."""
+    rng = np.random.default_rng(9)
+    T, d, E, k, F, Fs = 10, 8, 6, 3, 16, 8
+    x = f32(rng.standard_normal((T, d)))
+    one_gu = f32(rng.standard_normal((2 * F, d)) / 3)
+    one_dn = f32(rng.standard_normal((d, F)) / 4)
+    shg = f32(rng.standard_normal((2 * Fs, d)) / 3)
+    shd = f32(rng.standard_normal((d, Fs)) / 3)
+    wgu = np.stack([one_gu] * E); wd = np.stack([one_dn] * E)
+    l = rng.standard_normal((T, E))
+    idx, w, _ = oracle.topk(l, softmax(l, axis=1), k)
+    out = oracle.layer_rows(x, idx, w, wgu, wd, shg, shd)
+    xd = x.astype(np.float64)
+    dense = (silu(xd @ one_gu[:F].T.astype(np.float64)) * (xd @ one_gu[F:].T.astype(np.float64))) \
+        @ one_dn.T.astype(np.float64)
+    shared = (silu(xd @ shg[:Fs].T.astype(np.float64)) * (xd @ shg[Fs:].T.astype(np.float64))) \
+        @ shd.T.astype(np.float64)
+    np.testing.assert_allclose(out, dense + shared, rtol=1e-12, atol=1e-12)
+    idx2 = np.roll(idx, 1, axis=1)
+    np.testing.assert_allclose(oracle.layer_rows(x, idx2, w, wgu, wd, shg, shd), out,
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_missing_expert_weights_is_an_error():
+    x = f32([[1.0, 2.0]])
+    idx = np.array([[1]], dtype=np.int32)
+    w = np.array([[1.0]])
+    with pytest.raises(ValueError):
+        oracle.layer_rows(x, idx, w, {0: f32([[1, 0], [0, 1]])}, {0: f32([[1], [1]])})
