@@ -1,0 +1,157 @@
+/* moe_layer.h -- C ABI of the B300 (sm_103a) forward pass of one sparse Mixture-of-Experts
+ * FFN layer, single GPU.
+ *
+ * The operation (one layer, T tokens of width d, E routed experts, top-k):
+ *   1. router: logits = x * w_router^T, then a score per expert: softmax over the E logits,
+ *      or a sigmoid of each logit.  Page "Expert-Parallel MoE Inference: Serving Sparse Models
+ *      at Scale", section "Deeper Analysis: Routing, Balance, and a Capacity Worked Example":
+ *      a linear gate scores every expert for every token, a softmax is applied and the top-k
+ *      are kept.  The sigmoid form with a per-expert selection bias is the auxiliary-loss-free
+ *      balancing named on page "Expert Parallelism for MoE Serving", section "The Future of
+ *      Expert Parallelism for MoE Serving".
+ *   2. top-k: the k largest selection keys per token (key = logit for softmax, sigmoid score
+ *      for sigmoid, plus bias[e] when a bias is given); equal keys go to the lower expert id;
+ *      the k gate weights are the unbiased scores of the chosen experts, renormalised to sum
+ *      to one.
+ *   3. dispatch: assignments grouped by expert, token order kept within an expert -- the
+ *      one-GPU form of the dispatch all-to-all (page "Expert-Parallel MoE Inference", section
+ *      "The all-to-all dispatch and combine, step by step"; page "MoE Expert Parallelism in
+ *      Practice", "Core Principles" part 1).
+ *   4. experts: each routed expert is a SwiGLU FFN, W_down (silu(W_gate x) * (W_up x)), run as
+ *      a grouped GEMM over the expert segments (page "Tensor vs Expert vs Data Parallelism for
+ *      MoE Serving", Figure 2: experts run grouped GEMMs).  An optional shared expert of inner
+ *      width Fs sees every token with weight 1 (same page, "Context and Background": routed
+ *      experts plus a shared expert).
+ *   5. combine: out[t] = sum_j w_tj * y_(t,j) + y_shared[t], summed in a fixed order with no
+ *      floating-point atomics, so the output is bit-reproducible from run to run (page "MoE
+ *      Expert Parallelism in Practice", "Core Principles" part 1: outputs are combined and
+ *      mapped back to the original token order).
+ * The layer is drop-free: every assignment is computed (page "Expert-Parallel MoE
+ * Inference", "Capacity factor and token dropping": production inference prefers a
+ * drop-free path).
+ *
+ * Conventions for every entry point:
+ *   - Every array pointer is DEVICE memory owned by the caller, 16-byte aligned, row-major.
+ *     The library allocates no memory, keeps no per-call state and takes no ownership.
+ *   - All work is enqueued on `stream`; no call synchronises with the host (except
+ *     moe_workspace_status, which says so), so a forward pass can be captured in a CUDA graph.
+ *   - Errors are returned before anything is enqueued: MOE_ERR_INVALID_ARG for a null
+ *     required pointer, misaligned pointer or out-of-range size; MOE_ERR_UNSUPPORTED for a
+ *     shape the kernels do not handle; MOE_ERR_WORKSPACE for a workspace smaller than
+ *     moe_layer_workspace_size().  MOE_ERR_CUDA reports a failed launch or tensor-map
+ *     encode.  Kernels that time out on an internal wait record a code that
+ *     moe_workspace_status() returns as MOE_ERR_DEVICE (the kernel returns instead of
+ *     hanging).
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,
+  MOE_ERR_UNSUPPORTED = -2,
+  MOE_ERR_WORKSPACE = -3,
+  MOE_ERR_CUDA = -4,
+  MOE_ERR_DEVICE = -5
+};
+
+/* Limits: 1 <= k <= 32, k <= E <= 1024, T * k < 2^31.  For MOE_DTYPE_BF16 (tensor-core
+ * path, fp32 accumulation): d, F and Fs must be multiples of 64.  MOE_DTYPE_F32 runs every
+ * product in true fp32 (no TF32) on CUDA cores and has no shape restriction. */
+typedef struct {
+  int T;   /* tokens */
+  int d;   /* hidden width */
+  int E;   /* routed experts */
+  int k;   /* experts per token */
+  int F;   /* routed expert inner width */
+  int Fs;  /* shared expert inner width, 0 = no shared expert */
+  moe_dtype dtype; /* element type of x, all weights, out */
+} moe_shape;
+
+typedef struct {
+  const void* w_gate_up; /* [2*Fs][d]: rows 0..Fs-1 gate, rows Fs..2Fs-1 up (K-major) */
+  const void* w_down;    /* [d][Fs] */
+} moe_shared_expert;
+
+/* Bytes of device workspace moe_layer_forward and moe_route_from_keys need for this shape
+ * (worst case: the pass is drop-free, so R = T*k routed rows always fit).  0 if the shape is
+ * invalid. */
+size_t moe_layer_workspace_size(const moe_shape* s);
+
+/* One forward pass of the layer.
+ *   x         [T][d]          dtype
+ *   w_router  [E][d]          dtype; row e scores expert e
+ *   w_gate_up [E][2F][d]      dtype; per expert F gate rows then F up rows (K-major)
+ *   w_down    [E][d][F]       dtype (K-major)
+ *   score_fn  MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID
+ *   bias      [E] fp32 or NULL; added to the selection key only (never to the weights)
+ *   shared_expert  NULL when s->Fs == 0, else both pointers set
+ *   out       [T][d]          dtype, written
+ *   expert_counts [E] int32, written: tokens routed to each expert
+ *   workspace / workspace_bytes: at least moe_layer_workspace_size(s) bytes; its contents
+ *             are scratch between calls; calls that overlap on the GPU must not share it
+ *   topk_idx_out [T][k] int32, topk_w_out [T][k] fp32, sorted_token_out [T*k] int32: optional
+ *             (NULL to skip) copies of the routing (key-descending order) and of the dispatch
+ *             permutation (for each expert in id order, its tokens in ascending order).
+ * Returns MOE_OK or a negative MOE_ERR_* (see the conventions above). */
+int moe_layer_forward(const moe_shape* s, const void* x, const void* w_router,
+                      const void* w_gate_up, const void* w_down, moe_score_fn score_fn,
+                      const float* bias, const moe_shared_expert* shared_expert, void* out,
+                      int* expert_counts, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream, int* topk_idx_out, float* topk_w_out,
+                      int* sorted_token_out);
+
+/* Number of CUDA events moe_layer_forward_ex records when stage_events is given:
+ * [0] start, [1] router GEMM, [2] top-k, [3] histogram/scan/permutation, [4] gather,
+ * [5] gate/up grouped GEMM, [6] down grouped GEMM, [7] combine (each after its kernels). */
+#define MOE_NUM_STAGE_EVENTS 8
+
+typedef struct {
+  cudaEvent_t* stage_events; /* NULL, or MOE_NUM_STAGE_EVENTS events created by the caller */
+} moe_forward_opts;
+
+/* moe_layer_forward with options (stage timing events); opts may be NULL. */
+int moe_layer_forward_ex(const moe_shape* s, const void* x, const void* w_router,
+                         const void* w_gate_up, const void* w_down, moe_score_fn score_fn,
+                         const float* bias, const moe_shared_expert* shared_expert, void* out,
+                         int* expert_counts, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream, int* topk_idx_out, float* topk_w_out,
+                         int* sorted_token_out, const moe_forward_opts* opts);
+
+/* Routing and dispatch tables from supplied fp32 selection keys and gate scores (steps 2-3
+ * above with the scores given instead of computed), for bit-exact checks:
+ *   sel_key [T][E], gate_score [T][E] fp32
+ *   topk_idx [T][k], topk_w [T][k] = gate_score of the chosen, renormalised
+ *   expert_counts [E], expert_offsets [E+1] (exclusive prefix sum, last = T*k)
+ *   sorted_token [T*k], slot_pos [T][k] (position of assignment (t, j) in sorted order).
+ * s->d, s->F, s->Fs and s->dtype are ignored.  Returns MOE_OK or MOE_ERR_*. */
+int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* gate_score,
+                        int* topk_idx, float* topk_w, int* expert_counts, int* expert_offsets,
+                        int* sorted_token, int* slot_pos, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* Kernel launches one moe_layer_forward makes for this shape (for launch accounting). */
+int moe_layer_num_launches(const moe_shape* s);
+
+/* Reads the device status word of a workspace after the caller's work on it has finished:
+ * SYNCHRONOUS (cudaMemcpy).  *status = MOE_OK, or MOE_ERR_DEVICE if a kernel gave up on an
+ * internal wait; *detail = the raw code the kernel recorded (0 if none). */
+int moe_workspace_status(const void* workspace, int* status, int* detail);
+
+/* Static string for a status code. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_LAYER_H */

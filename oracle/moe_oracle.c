@@ -52,8 +52,9 @@ int oracle_router_scores(int n_tok, int d, int E, int dtype, const void* x_rows,
       if (logits) logits[o] = l[e];
       if (score) score[o] = s[e];
       if (key) {
-        if (score_fn == ORACLE_SOFTMAX) key[o] = l[e];  /* softmax is monotone in the logit */
-        else key[o] = s[e] + (bias ? (double)bias[e] : 0.0);
+        /* softmax is monotone in the logit, so the logit itself orders the experts */
+        double base = score_fn == ORACLE_SOFTMAX ? l[e] : s[e];
+        key[o] = base + (bias ? (double)bias[e] : 0.0);
       }
     }
   }

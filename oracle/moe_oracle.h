@@ -7,8 +7,8 @@
  *
  * What it computes (every sum in fp64, inputs converted exactly from fp32 / bf16):
  *   logits l[t][e] = sum_i x[t][i] * w_router[e][i]
- *   softmax: score = softmax over all E logits, key = logit
- *   sigmoid: score = 1 / (1 + exp(-l)),        key = score + bias[e]
+ *   softmax: score = softmax over all E logits, key = logit (+ bias[e] if given)
+ *   sigmoid: score = 1 / (1 + exp(-l)),        key = score (+ bias[e] if given)
  *   S_t = the k largest keys (ties -> lower expert id), in key-descending order
  *   w_tj = score[S_tj] / sum_j' score[S_tj']
  *   FFN_e(x) = W_down[e] (silu(W_gate[e] x) * (W_up[e] x)),  silu(g) = g / (1 + exp(-g))
@@ -46,7 +46,7 @@ enum { ORACLE_SOFTMAX = 0, ORACLE_SIGMOID = 1 };
 double oracle_elem(const void* base, int dtype, size_t i);
 
 /* Router logits, gate scores and selection keys for n_tok token rows.
- * x_rows [n_tok][d], w_router [E][d]; bias [E] fp32 or NULL (= 0, sigmoid only).
+ * x_rows [n_tok][d], w_router [E][d]; bias [E] fp32 or NULL (= 0): selection only.
  * logits, score, key: [n_tok][E] fp64, any may be NULL. */
 int oracle_router_scores(int n_tok, int d, int E, int dtype, const void* x_rows,
                          const void* w_router, int score_fn, const float* bias,

@@ -286,3 +286,17 @@ def test_missing_expert_weights_is_an_error():
     w = np.array([[1.0]])
     with pytest.raises(ValueError):
         oracle.layer_rows(x, idx, w, {0: f32([[1, 0], [0, 1]])}, {0: f32([[1], [1]])})
+
+
+def test_softmax_bias_moves_selection_not_weights():
+    """Softmax with a selection bias: key = logit + b selects, the weights stay the
+    renormalised unbiased softmax.  l=[2,1,0], b=[0,0,2.5]: keys [2,1,2.5];
+    k=2 -> (2, 0) with w = softmax([0, 2]) = (1/(1+e^2), 1/(1+e^-2))."""
+    x = f32([[1, 0]])
+    wr = f32([[2, 0], [1, 0], [0, 0]])
+    bias = f32([0, 0, 2.5])
+    _, s, key = oracle.router_scores(x, wr, oracle.SOFTMAX, bias)
+    idx, w, _ = oracle.topk(key, s, 2)
+    assert idx.tolist() == [[2, 0]]
+    assert w[0, 0] == pytest.approx(1 / (1 + math.exp(2)), abs=1e-15)
+    assert w[0, 1] == pytest.approx(1 / (1 + math.exp(-2)), abs=1e-15)
