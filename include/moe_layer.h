@@ -140,6 +140,17 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
                         int* sorted_token, int* slot_pos, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream);
 
+/* Diagnostics, host only (launches nothing): the tile schedule the bf16 grouped GEMM `which`
+ * (0 = router, 1 = gate/up, 2 = down) would run for the given per-expert token counts
+ * (host array [E]; ignored for the router) on a device with num_sms SMs.  Writes up to
+ * max_tiles rows of 7 ints {operand set (0 routed / 1 shared), segment, weight tile m, first
+ * token row, MMA N, rows that belong to the segment, loads second 64-row weight box} into
+ * tiles (host), and 8 ints {n-tile cap, pipeline stages, stage bytes, shared-memory bytes,
+ * m-tiles of set 0, m-tiles of set 1, m-group, K of set 0} into geometry (host, may be NULL).
+ * Returns the schedule's tile count (may exceed max_tiles) or a negative MOE_ERR_*. */
+int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,
+                         int* tiles, int max_tiles, int* geometry);
+
 /* Kernel launches one moe_layer_forward makes for this shape (for launch accounting). */
 int moe_layer_num_launches(const moe_shape* s);
 

@@ -1,0 +1,544 @@
+// C ABI of the MoE layer (declared in include/moe_layer.h): argument checks, the workspace
+// layout, tensor-map encoding and the launch sequence on the caller's stream.
+//
+// Sequence of one forward pass (all on `stream`, no host synchronisation):
+//   router GEMM -> top-k -> histogram / scan / stable permutation -> gather -> gate/up grouped
+//   GEMM (+SwiGLU) -> down grouped GEMM -> combine.
+// bf16 layers run the three GEMMs on the tensor cores (moe_gemm_tc.cu); fp32 layers run them
+// in true fp32 on CUDA cores (moe_router.cu, moe_ffn_simt.cu).  Routing, dispatch and combine
+// kernels are shared by both.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_layer.h"
+#include "moe_internal.h"
+#include "tile_sched.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  size_t status, logits, topk_idx, topk_w, chunk, offsets, ntp, sorted, slot, xs_y, h, h_sh, total;
+};
+
+// Workspace carve-up.  xs (gathered rows) and y (expert outputs, routed rows then the shared
+// expert's rows) share one region: xs is dead once the gate/up GEMM has consumed it.
+Layout layout_of(const moe_shape& s) {
+  const size_t elt = s.dtype == MOE_DTYPE_BF16 ? 2 : 4;
+  const size_t R = (size_t)s.T * s.k;
+  const size_t nch = (R + kDispatchChunk - 1) / kDispatchChunk;
+  const size_t tsh = s.Fs > 0 ? (size_t)s.T : 0;
+  Layout w;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  w.status = take(256);
+  w.logits = take((size_t)s.T * s.E * 4);
+  w.topk_idx = take(R * 4);
+  w.topk_w = take(R * 4);
+  w.chunk = take(nch * s.E * 4);
+  w.offsets = take((size_t)(s.E + 1) * 4);
+  w.ntp = take((size_t)(s.E + 1) * 4);
+  w.sorted = take(R * 4);
+  w.slot = take(R * 4);
+  w.xs_y = take((R + tsh) * s.d * elt);
+  w.h = take(R * s.F * elt);
+  w.h_sh = take(tsh * (size_t)s.Fs * elt);
+  w.total = o;
+  return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const moe_shape* s, bool routing_only) {
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;
+  if (s->T < 1 || s->E < 1 || s->k < 1 || s->k > s->E || s->k > kMaxK || s->E > kMaxE)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)s->T * s->k > INT_MAX / 2) return MOE_ERR_INVALID_ARG;
+  if (routing_only) return MOE_OK;
+  if (s->d < 1 || s->F < 1 || s->Fs < 0) return MOE_ERR_INVALID_ARG;
+  if (s->dtype != MOE_DTYPE_F32 && s->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  const long long R = (long long)s->T * s->k;
+  if ((R + s->T) * (long long)s->d > (1LL << 40) || R * (long long)s->F > (1LL << 40))
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)s->E * 2 * s->F > INT_MAX || (long long)s->E * s->d > INT_MAX)
+    return MOE_ERR_INVALID_ARG;
+  if (s->dtype == MOE_DTYPE_BF16 && (s->d % 64 != 0 || s->F % 64 != 0 || s->Fs % 64 != 0))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> g(mu);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+int pow2_at_least(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+int largest_group(int m_tiles) {
+  for (int g = 16; g > 1; g >>= 1)
+    if (m_tiles % g == 0) return g;
+  return 1;
+}
+
+// n-tile cap of the expert GEMMs: twice the mean rows per expert, 32..256.
+int expert_bn(const moe_shape& s) {
+  const long long R = (long long)s.T * s.k;
+  const int avg = (int)((R + s.E - 1) / s.E);
+  int bn = pow2_at_least(avg * 2 > 32 ? avg * 2 : 32);
+  return bn > 256 ? 256 : bn;
+}
+
+// n-tile cap of the router GEMM: about one tile per SM.
+int router_bn(const moe_shape& s, int sms) {
+  const int m_tiles = (s.E + 127) / 128;
+  const int nt_target = (sms + m_tiles - 1) / m_tiles;
+  int per = (s.T + nt_target - 1) / nt_target;
+  int bn = pow2_at_least(per < 16 ? 16 : per);
+  return bn > 256 ? 256 : bn;
+}
+
+int encode_tokens(TcProblem& P, const void* base, int rows, int cols) {
+  const uint32_t boxes[4] = {128, 64, 32, 16};
+  for (int b = 0; b < 4; ++b)
+    if (encode_tmap_bf16(&P.tmB[b], base, (uint64_t)rows, (uint64_t)cols, boxes[b]) != 0) return -1;
+  return 0;
+}
+
+struct Plan {
+  TcParams router, gateup, down;
+};
+
+// Tile geometry of the three GEMMs of a bf16 layer (everything but pointers and tensor maps).
+void geometry_router(const moe_shape& s, int sms, TcParams& p) {
+  memset(&p, 0, sizeof(p));
+  TcProblem& P = p.prob[0];
+  p.n_prob = 1;
+  p.bn = router_bn(s, sms);
+  P.a_box_rows = s.E < 64 ? s.E : 64;
+  P.K = s.d;
+  P.m_tiles = (s.E + 127) / 128;
+  P.group = largest_group(P.m_tiles);
+  P.a_seg_stride = 0;
+  P.a_m_stride = 128;
+  P.a_box1_off = 64;
+  P.a_valid_rows = s.E;
+  P.rows = s.T;
+  P.nt = (s.T + p.bn - 1) / p.bn;
+  P.out_ld = s.E;
+  P.out_valid_m = s.E;
+  p.stages = gemm_tc_plan_stages(p.bn, 0, &p.stage_bytes);
+}
+
+void geometry_gateup(const moe_shape& s, TcParams& p) {
+  memset(&p, 0, sizeof(p));
+  const int bn = expert_bn(s);
+  p.n_prob = s.Fs > 0 ? 2 : 1;
+  p.bn = bn;
+  TcProblem& P = p.prob[0];
+  P.a_box_rows = 64;
+  P.n_seg = s.E;
+  P.K = s.d;
+  P.m_tiles = s.F / 64;
+  P.group = largest_group(P.m_tiles);
+  P.a_seg_stride = 2 * s.F;
+  P.a_m_stride = 64;
+  P.a_box1_off = s.F;
+  P.a_valid_rows = INT_MAX;
+  P.out_ld = s.F;
+  P.out_valid_m = INT_MAX;
+  if (s.Fs > 0) {
+    TcProblem& Q = p.prob[1];
+    Q.a_box_rows = 64;
+    Q.K = s.d;
+    Q.m_tiles = s.Fs / 64;
+    Q.group = largest_group(Q.m_tiles);
+    Q.a_seg_stride = 0;
+    Q.a_m_stride = 64;
+    Q.a_box1_off = s.Fs;
+    Q.a_valid_rows = INT_MAX;
+    Q.rows = s.T;
+    Q.nt = (s.T + bn - 1) / bn;
+    Q.out_ld = s.Fs;
+    Q.out_valid_m = INT_MAX;
+  }
+  p.stages = gemm_tc_plan_stages(bn, s.E, &p.stage_bytes);
+}
+
+void geometry_down(const moe_shape& s, TcParams& p) {
+  memset(&p, 0, sizeof(p));
+  const int bn = expert_bn(s);
+  p.n_prob = s.Fs > 0 ? 2 : 1;
+  p.bn = bn;
+  TcProblem& P = p.prob[0];
+  P.a_box_rows = 64;
+  P.n_seg = s.E;
+  P.K = s.F;
+  P.m_tiles = (s.d + 127) / 128;
+  P.group = largest_group(P.m_tiles);
+  P.a_seg_stride = s.d;
+  P.a_m_stride = 128;
+  P.a_box1_off = 64;
+  P.a_valid_rows = s.d;
+  P.out_ld = s.d;
+  P.out_valid_m = s.d;
+  if (s.Fs > 0) {
+    TcProblem& Q = p.prob[1];
+    Q.a_box_rows = 64;
+    Q.K = s.Fs;
+    Q.m_tiles = (s.d + 127) / 128;
+    Q.group = largest_group(Q.m_tiles);
+    Q.a_seg_stride = 0;
+    Q.a_m_stride = 128;
+    Q.a_box1_off = 64;
+    Q.a_valid_rows = s.d;
+    Q.rows = s.T;
+    Q.nt = (s.T + bn - 1) / bn;
+    Q.out_ld = s.d;
+    Q.out_row_base = s.T * s.k;
+    Q.out_valid_m = s.d;
+  }
+  p.stages = gemm_tc_plan_stages(bn, s.E, &p.stage_bytes);
+}
+
+// Geometry plus operand pointers and tensor maps.
+int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const void* w_gate_up,
+              const void* w_down, const moe_shared_expert* sh, char* ws, const Layout& L,
+              int sms, Plan& pl) {
+  const int T = s.T, d = s.d, E = s.E, F = s.F, Fs = s.Fs;
+  const int R = T * s.k;
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  int* offsets = reinterpret_cast<int*>(ws + L.offsets);
+  int* ntp = reinterpret_cast<int*>(ws + L.ntp);
+  void* xs_y = ws + L.xs_y;
+  void* h = ws + L.h;
+  void* h_sh = ws + L.h_sh;
+
+  TcParams& pr = pl.router;
+  geometry_router(s, sms, pr);
+  pr.err = status;
+  pr.prob[0].out = ws + L.logits;
+  if (encode_tmap_bf16(&pr.prob[0].tmA, w_router, (uint64_t)E, (uint64_t)d,
+                       (uint32_t)pr.prob[0].a_box_rows) != 0 ||
+      encode_tokens(pr.prob[0], x, T, d) != 0)
+    return -1;
+
+  TcParams& pg = pl.gateup;
+  geometry_gateup(s, pg);
+  pg.err = status;
+  pg.prob[0].out = h;
+  pg.prob[0].seg_off = offsets;
+  pg.prob[0].ntp = ntp;
+  if (encode_tmap_bf16(&pg.prob[0].tmA, w_gate_up, (uint64_t)E * 2 * F, (uint64_t)d, 64) != 0 ||
+      encode_tokens(pg.prob[0], xs_y, R, d) != 0)
+    return -1;
+  if (Fs > 0) {
+    pg.prob[1].out = h_sh;
+    if (encode_tmap_bf16(&pg.prob[1].tmA, sh->w_gate_up, (uint64_t)2 * Fs, (uint64_t)d, 64) != 0 ||
+        encode_tokens(pg.prob[1], x, T, d) != 0)
+      return -1;
+  }
+
+  TcParams& pd = pl.down;
+  geometry_down(s, pd);
+  pd.err = status;
+  pd.prob[0].out = xs_y;
+  pd.prob[0].seg_off = offsets;
+  pd.prob[0].ntp = ntp;
+  if (encode_tmap_bf16(&pd.prob[0].tmA, w_down, (uint64_t)E * d, (uint64_t)F, 64) != 0 ||
+      encode_tokens(pd.prob[0], h, R, F) != 0)
+    return -1;
+  if (Fs > 0) {
+    pd.prob[1].out = xs_y;
+    if (encode_tmap_bf16(&pd.prob[1].tmA, sh->w_down, (uint64_t)d, (uint64_t)Fs, 64) != 0 ||
+        encode_tokens(pd.prob[1], h_sh, T, Fs) != 0)
+      return -1;
+  }
+  return 0;
+}
+
+int check_forward_args(const moe_shape* s, const void* x, const void* w_router,
+                       const void* w_gate_up, const void* w_down, int score_fn, const float* bias,
+                       const moe_shared_expert* sh, const void* out, const int* expert_counts,
+                       const void* workspace, size_t workspace_bytes, const int* topk_idx_out,
+                       const float* topk_w_out, const int* sorted_token_out) {
+  int rc = check_shape(s, false);
+  if (rc != MOE_OK) return rc;
+  if (!x || !w_router || !w_gate_up || !w_down || !out || !expert_counts || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (s->Fs > 0 && (sh == nullptr || sh->w_gate_up == nullptr || sh->w_down == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (s->Fs == 0 && sh != nullptr) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, w_router, w_gate_up, w_down, out, expert_counts, workspace, bias,
+                        topk_idx_out, topk_w_out, sorted_token_out,
+                        sh ? sh->w_gate_up : nullptr, sh ? sh->w_down : nullptr};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < layout_of(*s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int forward_impl(const moe_shape* s, const void* x, const void* w_router, const void* w_gate_up,
+                 const void* w_down, int score_fn, const float* bias,
+                 const moe_shared_expert* sh, void* out, int* expert_counts, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream, int* topk_idx_out,
+                 float* topk_w_out, int* sorted_token_out, const moe_forward_opts* opts) {
+  int rc = check_forward_args(s, x, w_router, w_gate_up, w_down, score_fn, bias, sh, out,
+                              expert_counts, workspace, workspace_bytes, topk_idx_out, topk_w_out,
+                              sorted_token_out);
+  if (rc != MOE_OK) return rc;
+  const int sms = device_sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const moe_shape& S = *s;
+  const Layout L = layout_of(S);
+  char* ws = static_cast<char*>(workspace);
+  const bool bf16 = S.dtype == MOE_DTYPE_BF16;
+  const int R = S.T * S.k;
+  const int tsh = S.Fs > 0 ? S.T : 0;
+  int* status = reinterpret_cast<int*>(ws + L.status);
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  int* tidx = topk_idx_out ? topk_idx_out : reinterpret_cast<int*>(ws + L.topk_idx);
+  float* tw = topk_w_out ? topk_w_out : reinterpret_cast<float*>(ws + L.topk_w);
+  int* chunk = reinterpret_cast<int*>(ws + L.chunk);
+  int* offsets = reinterpret_cast<int*>(ws + L.offsets);
+  int* ntp = reinterpret_cast<int*>(ws + L.ntp);
+  int* sorted = sorted_token_out ? sorted_token_out : reinterpret_cast<int*>(ws + L.sorted);
+  int* slot = reinterpret_cast<int*>(ws + L.slot);
+  void* xs_y = ws + L.xs_y;
+
+  Plan pl;
+  int bn = expert_bn(S);
+  if (bf16) {
+    if (plan_bf16(S, x, w_router, w_gate_up, w_down, sh, ws, L, sms, pl) != 0) return MOE_ERR_CUDA;
+    if (pl.router.stages < 2 || pl.gateup.stages < 2 || pl.down.stages < 2) return MOE_ERR_UNSUPPORTED;
+  }
+  cudaEvent_t* ev = opts ? opts->stage_events : nullptr;
+  auto mark = [&](int i) -> bool { return ev == nullptr || cudaEventRecord(ev[i], stream) == cudaSuccess; };
+  cudaError_t err = cudaSuccess;
+#define MOE_TRY(expr)                 \
+  do {                                \
+    err = (expr);                     \
+    if (err != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+  if (!mark(0)) return MOE_ERR_CUDA;
+  MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), stream));
+  if (bf16) MOE_TRY(launch_gemm_tc(kModeRouter, pl.router, sms, stream));
+  else MOE_TRY(launch_router_logits_f32(static_cast<const float*>(x), static_cast<const float*>(w_router),
+                                        S.T, S.d, S.E, logits, stream));
+  if (!mark(1)) return MOE_ERR_CUDA;
+  MOE_TRY(launch_topk(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, logits, nullptr, bias, S.T, S.E, S.k,
+                      tidx, tw, stream));
+  if (!mark(2)) return MOE_ERR_CUDA;
+  MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp, sorted, slot,
+                          stream));
+  if (!mark(3)) return MOE_ERR_CUDA;
+  MOE_TRY(launch_gather(x, sorted, R, S.d, bf16 ? 2 : 4, xs_y, stream));
+  if (!mark(4)) return MOE_ERR_CUDA;
+  if (bf16) {
+    MOE_TRY(launch_gemm_tc(kModeGateUp, pl.gateup, sms, stream));
+    if (!mark(5)) return MOE_ERR_CUDA;
+    MOE_TRY(launch_gemm_tc(kModeDown, pl.down, sms, stream));
+  } else {
+    MOE_TRY(launch_ffn_f32(static_cast<const float*>(xs_y), static_cast<const float*>(x), offsets,
+                           S.E, R, tsh, S.d, S.F, S.Fs, static_cast<const float*>(w_gate_up),
+                           static_cast<const float*>(w_down),
+                           sh ? static_cast<const float*>(sh->w_gate_up) : nullptr,
+                           sh ? static_cast<const float*>(sh->w_down) : nullptr,
+                           reinterpret_cast<float*>(ws + L.h), reinterpret_cast<float*>(ws + L.h_sh),
+                           nullptr, stream, 0));
+    if (!mark(5)) return MOE_ERR_CUDA;
+    MOE_TRY(launch_ffn_f32(nullptr, nullptr, offsets, S.E, R, tsh, S.d, S.F, S.Fs, nullptr,
+                           static_cast<const float*>(w_down), nullptr,
+                           sh ? static_cast<const float*>(sh->w_down) : nullptr,
+                           reinterpret_cast<float*>(ws + L.h), reinterpret_cast<float*>(ws + L.h_sh),
+                           static_cast<float*>(xs_y), stream, 1));
+  }
+  if (!mark(6)) return MOE_ERR_CUDA;
+  MOE_TRY(launch_combine(xs_y, slot, tw, S.T, S.k, S.d, R, S.Fs > 0 ? 1 : 0, bf16 ? 1 : 0, out, stream));
+  if (!mark(7)) return MOE_ERR_CUDA;
+#undef MOE_TRY
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_layer_workspace_size(const moe_shape* s) {
+  if (check_shape(s, false) != MOE_OK) return 0;
+  return layout_of(*s).total;
+}
+
+int moe_layer_forward(const moe_shape* s, const void* x, const void* w_router,
+                      const void* w_gate_up, const void* w_down, moe_score_fn score_fn,
+                      const float* bias, const moe_shared_expert* shared_expert, void* out,
+                      int* expert_counts, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream, int* topk_idx_out, float* topk_w_out,
+                      int* sorted_token_out) {
+  return forward_impl(s, x, w_router, w_gate_up, w_down, (int)score_fn, bias, shared_expert, out,
+                      expert_counts, workspace, workspace_bytes, stream, topk_idx_out, topk_w_out,
+                      sorted_token_out, nullptr);
+}
+
+int moe_layer_forward_ex(const moe_shape* s, const void* x, const void* w_router,
+                         const void* w_gate_up, const void* w_down, moe_score_fn score_fn,
+                         const float* bias, const moe_shared_expert* shared_expert, void* out,
+                         int* expert_counts, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream, int* topk_idx_out, float* topk_w_out,
+                         int* sorted_token_out, const moe_forward_opts* opts) {
+  if (opts != nullptr && opts->stage_events != nullptr)
+    for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
+      if (opts->stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  return forward_impl(s, x, w_router, w_gate_up, w_down, (int)score_fn, bias, shared_expert, out,
+                      expert_counts, workspace, workspace_bytes, stream, topk_idx_out, topk_w_out,
+                      sorted_token_out, opts);
+}
+
+int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* gate_score,
+                        int* topk_idx, float* topk_w, int* expert_counts, int* expert_offsets,
+                        int* sorted_token, int* slot_pos, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_shape(s, true);
+  if (rc != MOE_OK) return rc;
+  const void* ptrs[] = {sel_key, gate_score, topk_idx, topk_w, expert_counts, expert_offsets,
+                        sorted_token, slot_pos, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  // only the layout's leading tables (they depend on T, E and k alone) are used here
+  moe_shape r = *s;
+  r.d = 64;
+  r.F = 64;
+  r.Fs = 0;
+  r.dtype = MOE_DTYPE_BF16;
+  const Layout L = layout_of(r);
+  if (workspace_bytes < L.ntp + align256((size_t)(s->E + 1) * 4)) return MOE_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  if (launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, topk_idx, topk_w, stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
+                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp),
+                      sorted_token, slot_pos, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,
+                         int* tiles, int max_tiles, int* geometry) {
+  if (check_shape(s, false) != MOE_OK || s->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (which < 0 || which > 2 || num_sms < 1) return MOE_ERR_INVALID_ARG;
+  if (which > 0 && expert_counts == nullptr) return MOE_ERR_INVALID_ARG;
+  TcParams p;
+  if (which == 0) geometry_router(*s, num_sms, p);
+  else if (which == 1) geometry_gateup(*s, p);
+  else geometry_down(*s, p);
+  int* seg = nullptr;
+  int* ntp = nullptr;
+  int tiles0;
+  if (which > 0) {
+    seg = new int[s->E + 1];
+    ntp = new int[s->E + 1];
+    seg[0] = 0;
+    ntp[0] = 0;
+    for (int e = 0; e < s->E; ++e) {
+      if (expert_counts[e] < 0) {
+        delete[] seg;
+        delete[] ntp;
+        return MOE_ERR_INVALID_ARG;
+      }
+      seg[e + 1] = seg[e] + expert_counts[e];
+      ntp[e + 1] = ntp[e] + (expert_counts[e] + p.bn - 1) / p.bn;
+    }
+    p.prob[0].seg_off = seg;
+    p.prob[0].ntp = ntp;
+    tiles0 = ntp[s->E] * p.prob[0].m_tiles;
+  } else {
+    tiles0 = p.prob[0].nt * p.prob[0].m_tiles;
+  }
+  const int total = tiles0 + (p.n_prob > 1 ? p.prob[1].nt * p.prob[1].m_tiles : 0);
+  for (int t = 0; t < total && t < max_tiles; ++t) {
+    Tile tl;
+    decode_tile(p, seg, ntp, tiles0, t, tl);
+    int* o = tiles + 7 * (size_t)t;
+    o[0] = tl.prob;
+    o[1] = tl.seg;
+    o[2] = tl.m;
+    o[3] = tl.row0;
+    o[4] = tl.ncols;
+    o[5] = tl.valid;
+    o[6] = tile_has_box1(p.prob[tl.prob], tl) ? 1 : 0;
+  }
+  if (geometry) {
+    geometry[0] = p.bn;
+    geometry[1] = p.stages;
+    geometry[2] = p.stage_bytes;
+    geometry[3] = (int)gemm_tc_smem_bytes(p);
+    geometry[4] = p.prob[0].m_tiles;
+    geometry[5] = p.n_prob > 1 ? p.prob[1].m_tiles : 0;
+    geometry[6] = p.prob[0].group;
+    geometry[7] = p.prob[0].K;
+  }
+  delete[] seg;
+  delete[] ntp;
+  return total;
+}
+
+int moe_layer_num_launches(const moe_shape* s) {
+  if (check_shape(s, false) != MOE_OK) return -1;
+  // router, top-k, 3 dispatch kernels, gather, gate/up, down, combine
+  return 9;
+}
+
+int moe_workspace_status(const void* workspace, int* status, int* detail) {
+  if (workspace == nullptr || status == nullptr) return MOE_ERR_INVALID_ARG;
+  int code = 0;
+  if (cudaMemcpy(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *status = code == 0 ? MOE_OK : MOE_ERR_DEVICE;
+  if (detail) *detail = code;
+  return MOE_OK;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch or tensor-map error";
+    case MOE_ERR_DEVICE: return "a kernel gave up on an internal wait";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Host-side declarations shared by the kernel files and the C ABI layer (moe_api.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Codes a kernel records in the workspace status word when it gives up on a wait.
+enum DeviceErr {
+  kErrNone = 0,
+  kErrProducerWait = 1,
+  kErrMmaWait = 2,
+  kErrEpilogueWait = 3,
+  kErrDrainWait = 4,
+};
+
+// Epilogues of the tensor-core grouped GEMM.
+enum GemmMode { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
+
+// Assignments handled per block by the dispatch histogram / permutation kernels.
+constexpr int kDispatchChunk = 1024;
+constexpr int kDispatchWarps = 8;
+
+// One operand set of the persistent grouped GEMM.  "A" is always a weight matrix (the
+// MMA's M dimension, 128 rows per tile), "B" the token rows (the MMA's N dimension, a
+// multiple of 16 up to the n-tile cap), both K-major bf16 read through TMA with 128-byte
+// swizzle; the product is D = A * B^T accumulated in fp32 in tensor memory.
+struct TcProblem {
+  CUtensorMap tmA;     // weights [rows][K]: box 64 columns x a_box_rows rows
+  CUtensorMap tmB[4];  // tokens  [rows][K]: boxes of 128 / 64 / 32 / 16 rows x 64 columns
+  void* out;
+  const int* seg_off;  // grouped: device [n_seg+1] first B row of each segment; null = single
+  const int* ntp;      // grouped: device [n_seg+1] prefix of n-tiles per segment
+  int K;               // reduction length, multiple of 64
+  int m_tiles;         // 128-row weight tiles per segment
+  int group;           // m-tiles scheduled together (divides m_tiles)
+  int a_seg_stride;    // A rows between segments
+  int a_m_stride;      // A rows between m-tiles
+  int a_box1_off;      // A row offset of the second box of a tile
+  int a_valid_rows;    // second box is loaded only if (m * a_m_stride + a_box1_off) < this
+  int a_box_rows;      // rows per A box (64, or the whole A height when smaller)
+  int n_seg;           // grouped: number of segments
+  int rows;            // single segment: B rows
+  int nt;              // single segment: n-tiles
+  int out_ld;          // output row stride in elements
+  int out_row_base;    // output row of B row 0
+  int out_valid_m;     // weight rows that produce output (router: E, down: d)
+};
+
+struct TcParams {
+  TcProblem prob[2];
+  int n_prob;
+  int bn;           // n-tile cap: multiple of 16, at most 256
+  int stages;       // smem pipeline depth
+  int stage_bytes;  // 16 KiB A + bn * 128 B B
+  int* err;         // device status word
+};
+
+// Tensor-core GEMM (moe_gemm_tc.cu).
+size_t gemm_tc_smem_bytes(const TcParams& p);
+int gemm_tc_plan_stages(int bn, int n_seg, int* stage_bytes);
+cudaError_t launch_gemm_tc(int mode, const TcParams& p, int grid, cudaStream_t s);
+int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows);
+
+// Router (moe_router.cu).
+cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int T, int d, int E,
+                                     float* logits, cudaStream_t s);
+// src: 0 = logits + softmax, 1 = logits + sigmoid, 2 = supplied key (a) and score (b).
+cudaError_t launch_topk(int src, const float* a, const float* b, const float* bias, int T, int E,
+                        int k, int* topk_idx, float* topk_w, cudaStream_t s);
+
+// Dispatch (moe_dispatch.cu).
+cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
+                            int* expert_counts, int* offsets, int* ntp, int* sorted_token,
+                            int* slot_pos, cudaStream_t s);
+cudaError_t launch_gather(const void* x, const int* sorted_token, int R, int d, int elt_bytes,
+                          void* xs, cudaStream_t s);
+
+// fp32 expert FFN on CUDA cores (moe_ffn_simt.cu).
+cudaError_t launch_ffn_f32(const float* xs, const float* x, const int* offsets, int E, int R,
+                           int T_sh, int d, int F, int Fs, const float* w_gate_up,
+                           const float* w_down, const float* sh_gate_up, const float* sh_down,
+                           float* h, float* h_sh, float* y, cudaStream_t s, int stage);
+
+// Combine (moe_combine.cu).
+cudaError_t launch_combine(const void* y, const int* slot_pos, const float* topk_w, int T, int k,
+                           int d, int R, int has_shared, int bf16, void* out, cudaStream_t s);
+
+}  // namespace moe

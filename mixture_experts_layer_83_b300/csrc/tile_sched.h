@@ -1,0 +1,77 @@
+// Tile schedule of the persistent grouped GEMM, shared by the kernel (device) and the
+// diagnostics entry point (host) so that the host can check the exact index arithmetic the
+// kernel uses.
+#pragma once
+#include "moe_internal.h"
+
+#if defined(__CUDACC__)
+#define MOE_HD __host__ __device__ __forceinline__
+#else
+#define MOE_HD inline
+#endif
+
+namespace moe {
+
+struct Tile {
+  int prob;   // 0 = first operand set (grouped or single), 1 = second (single)
+  int seg;    // segment (expert) within the operand set
+  int m;      // 128-row weight tile index within the segment
+  int row0;   // first B row of the tile
+  int ncols;  // MMA N: multiple of 16, at most the n-tile cap
+  int valid;  // B rows of the tile that belong to the segment (<= ncols)
+};
+
+// Tile t of the schedule.  Operand set 0 comes first (tiles0 tiles), then set 1.  Within a
+// segment tiles run in (m-group, n-tile, m) order.  A segment of n rows is cut into nt n-tiles
+// of whole 16-row units, as even as possible.  `seg` / `ntp` are the segment row offsets and
+// the n-tile prefix of set 0 when it is grouped.
+MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, int tiles0, int t,
+                        Tile& tl) {
+  int prob = 0, local = t;
+  if (t >= tiles0) {
+    prob = 1;
+    local = t - tiles0;
+  }
+  const TcProblem& P = p.prob[prob];
+  const int M = P.m_tiles;
+  int seg = 0, nt, seg_row0 = 0, seg_rows;
+  if (prob == 0 && P.seg_off != nullptr) {
+    const int q = local / M;
+    int lo = 0, hi = P.n_seg;  // largest lo with ntp[lo] <= q
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ntp[mid] <= q) lo = mid;
+      else hi = mid;
+    }
+    seg = lo;
+    nt = ntp[seg + 1] - ntp[seg];
+    local -= ntp[seg] * M;
+    seg_row0 = seg_off[seg];
+    seg_rows = seg_off[seg + 1] - seg_row0;
+  } else {
+    nt = P.nt;
+    seg_rows = P.rows;
+  }
+  const int G = P.group;
+  const int mg = local / (G * nt);
+  const int r = local - mg * G * nt;
+  const int j = r / G;
+  tl.prob = prob;
+  tl.seg = seg;
+  tl.m = mg * G + (r - j * G);
+  const int units = (seg_rows + 15) >> 4;
+  const int q16 = units / nt, rem = units - q16 * nt;
+  const int u0 = j * q16 + (j < rem ? j : rem);
+  const int nu = q16 + (j < rem ? 1 : 0);
+  tl.row0 = seg_row0 + u0 * 16;
+  tl.ncols = nu * 16;
+  const int left = seg_rows - u0 * 16;
+  tl.valid = left < tl.ncols ? left : tl.ncols;
+}
+
+// Whether a tile loads the second 64-row weight box.
+MOE_HD bool tile_has_box1(const TcProblem& P, const Tile& tl) {
+  return P.a_box_rows == 64 && (tl.m * P.a_m_stride + P.a_box1_off) < P.a_valid_rows;
+}
+
+}  // namespace moe

@@ -1,0 +1,155 @@
+"""Parity helpers: run the layer through the C ABI on the GPU, compute the fp64 oracle on the
+same inputs, and compare them the way the layer's correctness criteria read:
+
+* routing: bit-exact top-k sets for every token whose k-th / (k+1)-th key margin (fp64 oracle
+  keys) is at least ``MARGIN``; a token under the margin may pick either side of the near-tie,
+  but its choice must be a valid top-k of the oracle keys up to ``MARGIN``;
+* dispatch tables: bit-exact against the oracle's tables for the GPU's routing;
+* output: max |err| <= 2e-2 * max |ref| and sum |err| / sum |ref| <= 5e-3 for bf16 (tighter
+  for fp32), the oracle evaluated under the GPU's routing, so an accepted near-tie does not
+  count as an output error.
+
+Test infrastructure: imports the oracle.
+"""
+import numpy as np
+
+import moe_inputs
+import oracle
+from moe_inputs import configs
+
+MARGIN = 1e-4
+TOL = {"bf16": dict(max_rel=2e-2, mean_rel=5e-3), "f32": dict(max_rel=1e-4, mean_rel=1e-5)}
+
+
+def moe_dtype(cfg):
+    import mixture_experts_layer_83_b300 as moe
+    return moe.MOE_DTYPE_BF16 if cfg["dtype"] == "bf16" else moe.MOE_DTYPE_F32
+
+
+def gpu_forward(cfg, dev, stream=None, workspace=None, stage_events=None):
+    """Run the layer on device tensors ``dev`` (from moe_inputs.device_inputs / upload)."""
+    import torch
+    import mixture_experts_layer_83_b300 as moe
+    c = configs.get(cfg)
+    T, d, E, k = c["T"], c["d"], c["E"], c["k"]
+    shape = moe.make_shape(T, d, E, k, c["F"], c["Fs"], moe_dtype(c))
+    ws_bytes = moe.moe_layer_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev["x"].device)
+    out = torch.empty_like(dev["x"])
+    counts = torch.empty(E, dtype=torch.int32, device=out.device)
+    tidx = torch.empty((T, k), dtype=torch.int32, device=out.device)
+    tw = torch.empty((T, k), dtype=torch.float32, device=out.device)
+    st = torch.empty(T * k, dtype=torch.int32, device=out.device)
+    shared = (dev["sh_gate_up"], dev["sh_down"]) if c["Fs"] > 0 else None
+    moe.moe_layer_forward(shape, dev["x"], dev["w_router"], dev["w_gate_up"], dev["w_down"],
+                          c["score"], dev.get("bias"), shared, out, counts, workspace, ws_bytes,
+                          stream, tidx, tw, st, stage_events=stage_events)
+    return dict(out=out, counts=counts, topk_idx=tidx, topk_w=tw, sorted_token=st,
+                workspace=workspace)
+
+
+def to_host(res):
+    import torch
+    h = {}
+    for key, v in res.items():
+        if key == "workspace":
+            continue
+        if v.dtype == torch.bfloat16:
+            h[key] = v.float().cpu().numpy().astype(np.float64)
+        else:
+            h[key] = v.cpu().numpy()
+    return h
+
+
+def oracle_routing(cfg, x, w_router, bias, threads=None):
+    """fp64 oracle logits -> (key, score, topk_idx, margin) for all rows of x (host arrays)."""
+    c = configs.get(cfg)
+
+    def part(lo, hi):
+        lg, sc, key = oracle.router_scores(x[lo:hi], w_router, c["score"], bias)
+        idx, _, margin = oracle.topk(key, sc, c["k"])
+        return key, sc, idx, margin
+
+    parts = oracle.parallel_rows(part, x.shape[0], threads=threads)
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(4))
+
+
+def check_routing(cfg, key, score, margin, o_idx, g_idx, g_w):
+    """Returns (n_excluded, oracle weights under the GPU's routing)."""
+    c = configs.get(cfg)
+    k = c["k"]
+    T = g_idx.shape[0]
+    assert g_idx.shape == (T, k)
+    assert np.all((g_idx >= 0) & (g_idx < c["E"])), "expert id out of range"
+    for t in range(T):
+        assert len(set(g_idx[t].tolist())) == k, f"token {t}: repeated expert"
+    excluded = margin < MARGIN
+    same = np.sort(g_idx, 1) == np.sort(o_idx, 1)
+    bad = np.where(~excluded & ~np.all(same, 1))[0]
+    assert bad.size == 0, f"{bad.size} tokens with margin >= {MARGIN} routed differently, e.g. " \
+        f"t={bad[0]} gpu={g_idx[bad[0]]} oracle={o_idx[bad[0]]} margin={margin[bad[0]]}"
+    rows = np.arange(T)[:, None]
+    sel_key = key[rows, g_idx]
+    masked = key.copy()
+    masked[rows, g_idx] = -np.inf
+    if k < c["E"]:
+        gap = sel_key.min(1) - masked.max(1)
+        assert np.all(gap >= -MARGIN), f"invalid near-tie choice, gap {gap.min()}"
+    # GPU order: non-increasing oracle key up to the margin
+    assert np.all(np.diff(sel_key, axis=1) <= MARGIN)
+    sc = score[rows, g_idx]
+    w_ref = sc / sc.sum(1, keepdims=True)
+    np.testing.assert_allclose(g_w, w_ref, rtol=0, atol=2e-5)
+    return int(excluded.sum()), w_ref
+
+
+def check_dispatch(cfg, g_idx, g_counts, g_sorted):
+    c = configs.get(cfg)
+    counts, offsets, st, _ = oracle.dispatch(g_idx.astype(np.int32), c["E"])
+    np.testing.assert_array_equal(g_counts, counts)
+    np.testing.assert_array_equal(g_sorted, st)
+    return counts
+
+
+def check_output(cfg, got, ref):
+    c = configs.get(cfg)
+    tol = TOL[c["dtype"]]
+    err = np.abs(got - ref)
+    max_ref = np.abs(ref).max()
+    max_rel = err.max() / max_ref
+    mean_rel = err.sum() / np.abs(ref).sum()
+    assert np.all(np.isfinite(got)), "non-finite output"
+    assert max_rel <= tol["max_rel"], f"max|err|/max|ref| = {max_rel:.3e}"
+    assert mean_rel <= tol["mean_rel"], f"sum|err|/sum|ref| = {mean_rel:.3e}"
+    return dict(max_rel=float(max_rel), mean_rel=float(mean_rel))
+
+
+def oracle_rows(cfg, x_rows, idx, w, experts, shared, threads=None):
+    """Oracle output rows under a routing; ``experts``: dict e -> (w_gate_up[e], w_down[e])."""
+    gu = {e: v[0] for e, v in experts.items()}
+    dn = {e: v[1] for e, v in experts.items()}
+    shg, shd = shared if shared is not None else (None, None)
+
+    def part(lo, hi):
+        return oracle.layer_rows(x_rows[lo:hi], idx[lo:hi], w[lo:hi], gu, dn, shg, shd)
+
+    return np.concatenate(oracle.parallel_rows(part, x_rows.shape[0], threads=threads, chunk=1))
+
+
+def full_check(cfg, dev=None, host=None, threads=None):
+    """Small shapes: GPU vs oracle on every token (host inputs uploaded byte-identically)."""
+    c = configs.get(cfg)
+    host = host if host is not None else moe_inputs.host_inputs(c)
+    dev = dev if dev is not None else moe_inputs.upload(c, host)
+    res = to_host(gpu_forward(c, dev))
+    key, score, o_idx, margin = oracle_routing(c, host["x"], host["w_router"], host.get("bias"),
+                                               threads)
+    n_ex, w_ref = check_routing(c, key, score, margin, o_idx, res["topk_idx"], res["topk_w"])
+    check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"])
+    experts = {e: (host["w_gate_up"][e], host["w_down"][e]) for e in range(c["E"])}
+    shared = (host["sh_gate_up"], host["sh_down"]) if c["Fs"] > 0 else None
+    ref = oracle_rows(c, host["x"], res["topk_idx"], w_ref, experts, shared, threads)
+    stats = check_output(c, res["out"], ref)
+    stats["excluded"] = n_ex
+    return stats

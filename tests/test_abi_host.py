@@ -1,0 +1,191 @@
+"""C ABI checks that need no GPU: exported symbols, argument validation (all decided on the
+host before anything is enqueued), workspace sizing and the grouped-GEMM tile schedule
+(computed by the library's own decoder, the code the kernel runs)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import mixture_experts_layer_83_b300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe_layer.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 8
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(moe.EXPORTED) == names
+
+
+def shape(T=64, d=128, E=8, k=2, F=128, Fs=0, dtype=moe.MOE_DTYPE_BF16):
+    return moe.make_shape(T, d, E, k, F, Fs, dtype)
+
+
+@pytest.mark.parametrize("bad", [dict(T=0), dict(E=0), dict(k=0), dict(k=9), dict(k=33, E=64),
+                                 dict(E=1025, k=2), dict(d=0), dict(F=0), dict(Fs=-1),
+                                 dict(dtype=7)])
+def test_workspace_size_rejects_invalid_shapes(bad):
+    assert moe.moe_layer_workspace_size(shape(**bad)) == 0
+
+
+def test_workspace_size_grows_with_the_problem():
+    a = moe.moe_layer_workspace_size(shape())
+    b = moe.moe_layer_workspace_size(shape(T=128))
+    c = moe.moe_layer_workspace_size(shape(Fs=64))
+    f = moe.moe_layer_workspace_size(shape(dtype=moe.MOE_DTYPE_F32))
+    assert 0 < a < b and a < c and a < f
+    R, d, F = 64 * 2, 128, 128
+    assert a >= R * d * 2 + R * F * 2 + 64 * 8 * 4
+
+
+def _forward(s, ptrs=None, ws_bytes=1 << 40, **kw):
+    p = dict(x=16, w_router=16, w_gate_up=16, w_down=16, out=16, expert_counts=16,
+             workspace=16, bias=None, shared=None)
+    p.update(ptrs or {})
+    return moe.moe_layer_forward(s, p["x"], p["w_router"], p["w_gate_up"], p["w_down"],
+                                 kw.get("score", moe.MOE_SCORE_SOFTMAX), p["bias"], p["shared"],
+                                 p["out"], p["expert_counts"], p["workspace"], ws_bytes, stream=0,
+                                 check=False)
+
+
+@pytest.mark.parametrize("field", ["x", "w_router", "w_gate_up", "w_down", "out", "expert_counts",
+                                   "workspace"])
+def test_forward_rejects_null_pointers(field):
+    assert _forward(shape(), {field: None}) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_forward_rejects_misaligned_pointers():
+    assert _forward(shape(), {"x": 18}) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(shape(), {"bias": 20}) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_forward_rejects_bad_score_fn_and_shared_expert_mismatch():
+    assert _forward(shape(), score=3) == moe.MOE_ERR_INVALID_ARG
+    assert _forward(shape(Fs=64)) == moe.MOE_ERR_INVALID_ARG            # shared weights missing
+    assert _forward(shape(), {"shared": (16, 16)}) == moe.MOE_ERR_INVALID_ARG  # Fs == 0
+    assert _forward(shape(Fs=64), {"shared": (16, None)}) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_forward_rejects_shapes_the_tensor_core_path_does_not_take():
+    assert _forward(shape(d=100)) == moe.MOE_ERR_UNSUPPORTED
+    assert _forward(shape(F=96)) == moe.MOE_ERR_UNSUPPORTED
+    assert _forward(shape(Fs=32), {"shared": (16, 16)}) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_forward_rejects_a_small_workspace():
+    s = shape()
+    need = moe.moe_layer_workspace_size(s)
+    assert _forward(s, ws_bytes=need - 1) == moe.MOE_ERR_WORKSPACE
+
+
+def test_route_from_keys_argument_checks():
+    s = shape()
+    args = [16] * 8   # fake addresses: every call below must be rejected before any launch
+    bad = list(args)
+    bad[2] = None
+    assert moe.moe_route_from_keys(s, *bad, 16, 1 << 30, stream=0,
+                                   check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_route_from_keys(shape(k=9), *args, 16, 1 << 30, stream=0,
+                                   check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_route_from_keys(s, *args, 16, 64, stream=0,
+                                   check=False) == moe.MOE_ERR_WORKSPACE
+
+
+def test_status_strings_and_launch_count():
+    assert moe.moe_status_string(0) == "ok"
+    assert "workspace" in moe.moe_status_string(moe.MOE_ERR_WORKSPACE)
+    assert moe.moe_layer_num_launches(shape()) == 9
+    assert moe.moe_layer_num_launches(shape(T=0)) == -1
+
+
+# ------------------------------------------------------------------ tile schedule
+def _check_schedule(s, which, counts):
+    tiles, geo = moe.moe_debug_gemm_tiles(s, which, counts)
+    assert 2 <= geo["stages"] <= 8
+    assert geo["smem_bytes"] <= 232448
+    assert geo["stage_bytes"] == 16384 + geo["bn"] * 128
+    bn = geo["bn"]
+    assert bn % 16 == 0 and 16 <= bn <= 256
+    if which == 0:
+        seg_rows = [s.T]
+        seg_off = [0, s.T]
+        m_tiles = [(s.E + 127) // 128]
+    else:
+        seg_rows = list(counts)
+        seg_off = np.concatenate([[0], np.cumsum(counts)])
+        m_tiles = [geo["m_tiles0"], geo["m_tiles1"]]
+    covered = {}
+    for prob, seg, m, row0, ncols, valid, box1 in tiles.tolist():
+        assert ncols % 16 == 0 and 16 <= ncols <= bn
+        assert 1 <= valid <= ncols
+        assert 0 <= m < m_tiles[prob]
+        if prob == 0:
+            lo, hi = seg_off[seg], seg_off[seg + 1]
+        else:
+            lo, hi = 0, s.T
+        assert lo <= row0 and row0 + valid <= hi
+        assert row0 + valid == hi or valid == ncols
+        for r in range(row0, row0 + valid):
+            key = (prob, seg, m, r)
+            assert key not in covered, key
+            covered[key] = 1
+        if which == 2:   # down: second box only while inside the d rows of the expert
+            assert box1 == (m * 128 + 64 < s.d)
+        elif which == 1:
+            assert box1 == 1
+        else:
+            assert box1 == (s.E >= 64 and m * 128 + 64 < s.E)
+    want = sum(m_tiles[0] * n for n in seg_rows)
+    if which > 0 and s.Fs > 0:
+        want += m_tiles[1] * s.T
+    assert len(covered) == want
+
+
+@pytest.mark.parametrize("which", [1, 2])
+@pytest.mark.parametrize("case", ["uniform", "ragged", "one_hot", "decode", "shared"])
+def test_expert_gemm_schedule_covers_every_row_once(which, case):
+    rng = np.random.default_rng(["uniform", "ragged", "one_hot", "decode", "shared"].index(case) * 10 + which)
+    if case == "uniform":
+        s = shape(T=512, d=256, E=16, k=4, F=192)
+        counts = np.full(16, 512 * 4 // 16)
+    elif case == "ragged":
+        s = shape(T=700, d=320, E=24, k=3, F=128)
+        counts = rng.multinomial(700 * 3, np.ones(24) / 24)
+        counts[3] = counts[3] + counts[5]
+        counts[5] = 0
+    elif case == "one_hot":
+        s = shape(T=1000, d=128, E=8, k=1, F=64)
+        counts = np.zeros(8, dtype=int)
+        counts[6] = 1000
+    elif case == "decode":
+        s = shape(T=128, d=7168, E=256, k=8, F=2048, Fs=2048)
+        counts = rng.multinomial(128 * 8, np.ones(256) / 256)
+    else:
+        s = shape(T=333, d=192, E=5, k=2, F=64, Fs=128)
+        counts = rng.multinomial(333 * 2, np.ones(5) / 5)
+    _check_schedule(s, which, counts)
+
+
+@pytest.mark.parametrize("T,E", [(1, 8), (37, 8), (300, 100), (8192, 256), (128, 256), (64, 1)])
+def test_router_gemm_schedule_covers_every_row_once(T, E):
+    _check_schedule(shape(T=T, E=E, k=1, d=256), 0, None)
+
+
+def test_prefill_geometry_uses_full_width_tiles():
+    s = shape(T=8192, d=7168, E=256, k=8, F=2048, Fs=2048)
+    _, geo = moe.moe_debug_gemm_tiles(s, 1, np.full(256, 256))
+    assert geo["bn"] == 256 and geo["stages"] == 4 and geo["m_tiles0"] == 32
+    _, geo = moe.moe_debug_gemm_tiles(shape(T=128, d=7168, E=256, k=8, F=2048, Fs=2048), 1,
+                                      np.full(256, 4))
+    assert geo["bn"] == 32 and geo["stages"] == 8

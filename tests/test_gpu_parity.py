@@ -1,0 +1,137 @@
+"""GPU parity through the C ABI against the fp64 oracle, at sizes the oracle finishes in
+seconds but that span several tiles and ragged tails, plus the degenerate cases."""
+import numpy as np
+import pytest
+
+import moe_inputs
+import oracle
+from moe_inputs import configs
+from moe_inputs.configs import SIGMOID, SOFTMAX, make_shape
+
+from layer_check import check_dispatch, full_check, gpu_forward, to_host
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixture_experts_layer_83_b300 as moe
+    moe.lib()
+
+
+SMALL = {
+    # several m-tiles, ragged expert segments, shared expert, sigmoid + bias
+    "bf16_sigmoid_shared": make_shape(300, 256, 16, 4, 192, Fs=128, score=SIGMOID,
+                                      bias_range=0.01, seed=11),
+    # d % 128 == 64: the down GEMM's last weight tile is half empty
+    "bf16_softmax_half_tile": make_shape(517, 192, 8, 2, 320, seed=12),
+    # 256 experts, ~6 rows each (decode-like segments), E not a multiple of 128 in the router
+    "bf16_many_experts": make_shape(200, 128, 200, 8, 64, Fs=64, score=SIGMOID, bias_range=0.01,
+                                    seed=13),
+    # segments longer than the 256-row n-tile cap
+    "bf16_long_segments": make_shape(600, 384, 4, 2, 256, seed=17),
+    "bf16_single_expert": make_shape(77, 128, 1, 1, 128, seed=14),
+    "bf16_k_equals_E": make_shape(40, 64, 6, 6, 64, seed=15),
+    "bf16_single_token": make_shape(1, 256, 32, 4, 128, Fs=64, score=SIGMOID, bias_range=0.01,
+                                    seed=16),
+    "bf16_k32": make_shape(50, 128, 64, 32, 64, seed=19),
+    "f32_tiny_config": configs.CONFIGS[0],
+    "f32_ragged": make_shape(99, 70, 5, 2, 33, Fs=17, dtype="f32", score=SIGMOID, bias_range=0.05,
+                             seed=18),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_matches_oracle(name):
+    stats = full_check(SMALL[name])
+    print(name, stats)
+
+
+def test_hot_experts_and_many_empty_experts():
+    """A large bias sends every token to experts 2 and 5: two segments of T rows each, all
+    other segments empty."""
+    cfg = make_shape(700, 128, 12, 2, 128, Fs=64, score=SIGMOID, bias_range=0.01, seed=21)
+    host = moe_inputs.host_inputs(cfg)
+    host["bias"] = host["bias"].copy()
+    host["bias"][[2, 5]] = 5.0
+    stats = full_check(cfg, host=host)
+    assert stats["excluded"] == 0
+
+
+def test_output_is_bit_reproducible():
+    cfg = SMALL["bf16_sigmoid_shared"]
+    dev = moe_inputs.upload(cfg, moe_inputs.host_inputs(cfg))
+    a = to_host(gpu_forward(cfg, dev))
+    b = to_host(gpu_forward(cfg, dev))
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_workspace_status_is_clean_after_a_pass():
+    import mixture_experts_layer_83_b300 as moe
+    cfg = SMALL["bf16_many_experts"]
+    dev = moe_inputs.upload(cfg, moe_inputs.host_inputs(cfg))
+    res = gpu_forward(cfg, dev)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_status(res["workspace"]) == (moe.MOE_OK, 0)
+
+
+# ------------------------------------------------------------------ bit-exact routing
+def _oracle_keys(T, E, score, seed, ties):
+    """fp32 selection keys and gate scores derived from oracle fp64 logits of synthetic rows."""
+    cfg = make_shape(T, 64, E, 1, 64, score=score, bias_range=0.01 if score == SIGMOID else 0.0,
+                     seed=seed)
+    x = moe_inputs.host_tensor(cfg, "x")
+    wr = moe_inputs.host_tensor(cfg, "w_router")
+    lg, sc, _ = oracle.router_scores(x, wr, score)
+    if score == SIGMOID:
+        b = moe_inputs.host_tensor(cfg, "bias")
+        key = sc.astype(np.float32) + b            # fp32 key = fp32(sigma) + b, in fp32
+    else:
+        key = lg.astype(np.float32)
+    if ties:
+        key = (np.round(key * 8) / 8).astype(np.float32)
+    return np.ascontiguousarray(key, np.float32), np.ascontiguousarray(sc, np.float32)
+
+
+@pytest.mark.parametrize("T,E,k,score,ties", [(1000, 256, 8, SIGMOID, False),
+                                              (4096, 8, 2, SOFTMAX, True),
+                                              (333, 1024, 32, SIGMOID, True),
+                                              (2500, 128, 8, SOFTMAX, True),
+                                              (64, 64, 64, SOFTMAX, False),
+                                              (3000, 33, 5, SIGMOID, True),
+                                              (1, 7, 3, SOFTMAX, True)])
+def test_route_from_keys_is_bit_exact(T, E, k, score, ties):
+    import mixture_experts_layer_83_b300 as moe
+    key, sc = _oracle_keys(T, E, score, seed=T + E + k, ties=ties)
+    o_idx, o_w, _ = oracle.topk(key.astype(np.float64), sc.astype(np.float64), k)
+    o_counts, o_off, o_st, o_sp = oracle.dispatch(o_idx, E)
+    dev = "cuda"
+    kk, ss = torch.from_numpy(key).to(dev), torch.from_numpy(sc).to(dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    st = torch.empty(T * k, dtype=torch.int32, device=dev)
+    sp = torch.empty((T, k), dtype=torch.int32, device=dev)
+    shape = moe.make_shape(T, 64, E, k, 64)
+    ws = torch.empty(moe.moe_layer_workspace_size(shape), dtype=torch.uint8, device=dev)
+    moe.moe_route_from_keys(shape, kk, ss, idx, w, counts, off, st, sp, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), o_idx)
+    np.testing.assert_array_equal(counts.cpu().numpy(), o_counts)
+    np.testing.assert_array_equal(off.cpu().numpy(), o_off)
+    np.testing.assert_array_equal(st.cpu().numpy(), o_st)
+    np.testing.assert_array_equal(sp.cpu().numpy(), o_sp)
+    np.testing.assert_allclose(w.cpu().numpy(), o_w, rtol=2e-6, atol=1e-7)
+
+
+def test_forward_dispatch_tables_match_oracle_for_gpu_routing():
+    cfg = SMALL["bf16_many_experts"]
+    dev = moe_inputs.upload(cfg, moe_inputs.host_inputs(cfg))
+    res = to_host(gpu_forward(cfg, dev))
+    counts = check_dispatch(cfg, res["topk_idx"], res["counts"], res["sorted_token"])
+    assert counts.sum() == cfg["T"] * cfg["k"]
