@@ -101,7 +101,7 @@ def _oracle_keys(T, E, score, seed, ties):
                                               (4096, 8, 2, SOFTMAX, True),
                                               (333, 1024, 32, SIGMOID, True),
                                               (2500, 128, 8, SOFTMAX, True),
-                                              (64, 64, 64, SOFTMAX, False),
+                                              (64, 32, 32, SOFTMAX, False),
                                               (3000, 33, 5, SIGMOID, True),
                                               (1, 7, 3, SOFTMAX, True)])
 def test_route_from_keys_is_bit_exact(T, E, k, score, ties):
