@@ -1,0 +1,493 @@
+"""Benchmark of the single-GPU MoE layer forward pass (one JSON line on rank 0).
+
+Default workload: the DeepSeek-V3-shaped prefill layer (T=8192 tokens, d=7168, 256 routed
+experts of inner width 2048 plus one shared expert, top-8, sigmoid scores with a selection
+bias), bf16 with fp32 accumulation, on synthetic seeded inputs resident in HBM.  A step is one
+full forward pass (router GEMM, top-k, dispatch, gather, gate/up GEMM + SwiGLU, down GEMM,
+combine).  The decode-shaped layer (T=128, same shapes) is measured the same way and
+reported under "decode".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+
+Under torchrun each rank runs an independent replica on its own tokens (data parallel, no
+collective on the data path); the time is the max over ranks and the value counts the tokens
+of all ranks.  ``--impl reference`` times the fp64 CPU oracle (the reference of this build)
+on a bounded sample of the same workload, on rank 0 only.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_inputs import configs  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# oracle sample sizes (tokens) giving roughly 10-30 s of single-core fp64 work
+CPU_SAMPLE = {0: 64, 1: 16, 2: 12, 3: 12, 4: 32}
+REF_SAMPLE = {0: 64, 1: 4, 2: 3, 3: 3, 4: 8}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def layer_flops(c):
+    """Active-parameter FLOPs of one pass: router + k routed experts + shared expert."""
+    T, d, E, k, F, Fs = c["T"], c["d"], c["E"], c["k"], c["F"], c["Fs"]
+    return T * (2 * d * E + 6 * d * F * k + 6 * d * Fs)
+
+
+def layer_bytes(c, counts):
+    """Bytes the method must move: x, router weights, touched experts, shared expert, out."""
+    s = 2 if c["dtype"] == "bf16" else 4
+    T, d, E, F, Fs = c["T"], c["d"], c["E"], c["F"], c["Fs"]
+    touched = int((np.asarray(counts) > 0).sum())
+    return T * d * s + E * d * s + touched * 3 * d * F * s + 3 * d * Fs * s + T * d * s
+
+
+def gateup_flops(c):
+    T, d, k, F, Fs = c["T"], c["d"], c["k"], c["F"], c["Fs"]
+    return 2 * d * (T * k * 2 * F + T * 2 * Fs)
+
+
+def gateup_weight_bytes(c, counts):
+    touched = int((np.asarray(counts) > 0).sum())
+    return 2 * (touched * 2 * c["F"] * c["d"] + 2 * c["Fs"] * c["d"])
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, kept for the timed region."""
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(1.0)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        note = None
+        if not inside:
+            inside = sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
+            note = "timed region shorter than the sampling period: nearest samples used"
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        out = {"sm_mhz": float(np.median([r[1] for r in inside])),
+               "sm_max_mhz": float(max(r[2] for r in inside)), "reasons": reasons,
+               "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value, world):
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def rank_inputs(c, rank):
+    """Model weights are shared by all replicas; each rank draws its own tokens."""
+    import moe_inputs
+    dev = moe_inputs.device_inputs(c)
+    if rank > 0:
+        dev["x"] = moe_inputs.device_tensor(dict(c, seed=c["seed"] + 7919 * rank), "x")
+    return dev
+
+
+class Runner:
+    """Device buffers and one-step closures for a config."""
+
+    def __init__(self, c, dev):
+        import torch
+        import mixture_experts_layer_83_b300 as moe
+        self.moe, self.torch, self.c, self.dev = moe, torch, c, dev
+        T, d, E, k = c["T"], c["d"], c["E"], c["k"]
+        dt = moe.MOE_DTYPE_BF16 if c["dtype"] == "bf16" else moe.MOE_DTYPE_F32
+        self.shape = moe.make_shape(T, d, E, k, c["F"], c["Fs"], dt)
+        self.ws_bytes = moe.moe_layer_workspace_size(self.shape)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty_like(dev["x"])
+        self.counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        self.shared = (dev["sh_gate_up"], dev["sh_down"]) if c["Fs"] > 0 else None
+        self.stream = torch.cuda.current_stream()
+        self.launches = moe.moe_layer_num_launches(self.shape)
+
+    def step(self, x=None, events=None):
+        d = self.dev
+        self.moe.moe_layer_forward(self.shape, d["x"] if x is None else x, d["w_router"],
+                                   d["w_gate_up"], d["w_down"], self.c["score"], d.get("bias"),
+                                   self.shared, self.out, self.counts, self.ws, self.ws_bytes,
+                                   self.stream, stage_events=events)
+
+    def timed(self, steps, warmup, world, with_stages=True):
+        torch = self.torch
+        nst = self.moe.MOE_NUM_STAGE_EVENTS
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(steps)]
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        start.record(self.stream)
+        for i in range(steps):
+            self.step(events=evs[i] if with_stages else None)
+        stop.record(self.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        ms = start.elapsed_time(stop) / steps
+        stages = None
+        if with_stages:
+            per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nst - 1)]
+                            for i in range(steps)])
+            stages = per.mean(0)
+        return ms, stages, (t0, t1)
+
+    def timed_e2e(self, steps, warmup, world):
+        """Host (pinned) x -> device, forward, device out + counts -> host, every step."""
+        torch = self.torch
+        x_host = self.dev["x"].cpu().pin_memory()
+        out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        cnt_host = torch.empty(self.counts.shape, dtype=torch.int32).pin_memory()
+        x_dev = torch.empty_like(self.dev["x"])
+
+        def one():
+            x_dev.copy_(x_host, non_blocking=True)
+            self.step(x=x_dev)
+            out_host.copy_(self.out, non_blocking=True)
+            cnt_host.copy_(self.counts, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        barrier(world)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(self.stream)
+        for _ in range(steps):
+            one()
+        stop.record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = start.elapsed_time(stop) / steps
+        h2d = x_host.numel() * x_host.element_size()
+        d2h = out_host.numel() * out_host.element_size() + cnt_host.numel() * 4
+        return ms, h2d, d2h
+
+
+def traffic_record(kernel):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source is unchanged."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for f in rec.get("sources", []):
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return rec["bytes_per_launch"] if h.hexdigest() == rec.get("sha256") else None
+
+
+def cpu_oracle_sample(c, dev, ntok, rank_seed_note=""):
+    """Time the oracle (single thread, as it stands) on the first ``ntok`` tokens of the
+    workload: router scores, top-k, routed experts, shared expert, combine."""
+    import torch
+    import oracle
+    oracle.build()
+    bf = c["dtype"] == "bf16"
+
+    def host(t):
+        t = t.contiguous()
+        return t.view(torch.int16).cpu().numpy().view(np.uint16) if bf else t.cpu().numpy()
+
+    x = host(dev["x"][:ntok])
+    wr = host(dev["w_router"])
+    bias = dev["bias"].cpu().numpy() if "bias" in dev else None
+    # experts the sample needs (input plumbing, outside the timed region)
+    _, sc, key = oracle.router_scores(x, wr, c["score"], bias)
+    idx, _, _ = oracle.topk(key, sc, c["k"])
+    experts = sorted(set(idx.ravel().tolist()))
+    gu = {e: host(dev["w_gate_up"][e]) for e in experts}
+    dn = {e: host(dev["w_down"][e]) for e in experts}
+    shg = host(dev["sh_gate_up"]) if c["Fs"] > 0 else None
+    shd = host(dev["sh_down"]) if c["Fs"] > 0 else None
+    t0 = time.perf_counter()
+    _, sc, key = oracle.router_scores(x, wr, c["score"], bias)
+    idx, w, _ = oracle.topk(key, sc, c["k"])
+    oracle.layer_rows(x, idx, w, gu, dn, shg, shd)
+    dt = time.perf_counter() - t0
+    return ntok / dt, dt
+
+
+def run_reference(args, c):
+    world, rank, local = dist_info()
+    if rank != 0:
+        return 0
+    import torch
+    torch.cuda.set_device(local)
+    import moe_inputs
+    dev = moe_inputs.device_inputs(c)
+    torch.cuda.synchronize()
+    n = REF_SAMPLE[args.config]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(c, dev, n)
+    times = [cpu_oracle_sample(c, dev, n)[1] for _ in range(args.steps)]
+    t = float(np.sum(times))
+    value = n * args.steps / t
+    line = {"impl": "reference", "metric": "MoE-layer tokens/s (fp64 CPU oracle)", "value": value,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(c),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} tokens per step (first {n} of the batch), router + "
+                                       f"top-k + routed and shared experts + combine"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(c):
+    return {"workload": f"{c['name']}: T={c['T']} d={c['d']} E={c['E']} top-{c['k']} "
+                        f"F={c['F']} shared Fs={c['Fs']} "
+                        f"{'sigmoid+bias' if c['score'] == configs.SIGMOID else 'softmax'} "
+                        f"{c['dtype']} seed={c['seed']}",
+            "T": c["T"], "d": c["d"], "E": c["E"], "k": c["k"], "F": c["F"], "Fs": c["Fs"],
+            "l2": "inputs larger than L2 (every step streams the touched expert weights, "
+                  "GBs per step, through a 126 MB L2)",
+            "parallelism": "replicas (data parallel, no collective on the data path)"}
+
+
+def measure(c, args, world, rank, peaks, sampler, kind):
+    import torch
+    dev = rank_inputs(c, rank)
+    torch.cuda.synchronize()
+    r = Runner(c, dev)
+    ms, stages, (t0, t1) = r.timed(args.steps, args.warmup, world)
+    ms_max = max_over_ranks(ms, world)
+    counts = r.counts.cpu().numpy()
+    res = {"ms": ms_max, "ms_local": ms, "stages": stages, "t0": t0, "t1": t1, "counts": counts,
+           "runner": r, "dev": dev}
+    fl = layer_flops(c)
+    by = layer_bytes(c, counts)
+    t_roof = max(fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
+    res["layer"] = {"tflops": fl / (ms_max * 1e-3) / 1e12, "gbs": by / (ms_max * 1e-3) / 1e9,
+                    "flop": fl, "bytes": by, "roofline_ms": t_roof * 1e3,
+                    "roofline_frac": t_roof * 1e3 / ms_max,
+                    "bound": "tensor" if fl / (peaks["bf16_tflops"] * 1e12) >=
+                    by / (peaks["hbm_gbs"] * 1e9) else "hbm"}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--decode-config", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=int, default=None, help="override tokens (profiling cases)")
+    ap.add_argument("--E", type=int, default=None, help="override routed experts (profiling)")
+    ap.add_argument("--profile", action="store_true",
+                    help="only warm-up + timed steps of the main workload (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    c = dict(configs.CONFIGS[args.config])
+    if args.T is not None or args.E is not None:
+        c["T"] = args.T or c["T"]
+        c["E"] = args.E or c["E"]
+        c["name"] = f"{c['name']} (T={c['T']}, E={c['E']} profiling case)"
+    if args.profile:
+        return run_profile(args, c)
+    if args.impl == "reference":
+        return run_reference(args, c)
+
+    world, rank, local = dist_info()
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import mixture_experts_layer_83_b300 as moe
+    moe.lib()
+    peaks, peak_src = load_peaks()
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    main_res = measure(c, args, world, rank, peaks, sampler, "prefill")
+    r = main_res["runner"]
+    e2e_ms, h2d, d2h = r.timed_e2e(args.steps, args.warmup, world)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    dc = configs.CONFIGS[args.decode_config]
+    del main_res["runner"], r
+    torch.cuda.empty_cache()
+    dec = measure(dc, args, world, rank, peaks, sampler, "decode")
+    if rank == 0:
+        sampler.stop()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    ms = main_res["ms"]
+    T = c["T"]
+    value = T * world / (ms * 1e-3)
+    st = main_res["stages"]
+    names = moe.STAGE_NAMES
+    gu_ms = float(st[names.index("gateup_gemm")])
+    gu_fl = gateup_flops(c)
+    achieved = gu_fl / (gu_ms * 1e-3) / 1e12
+    traffic = traffic_record("gemm_gateup_prefill")
+    roof = {"kernel": "gemm_tc_kernel<gate/up+SwiGLU> (tcgen05)", "bound": "tensor",
+            "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+            "peak_source": f"{peak_src} bf16 burst",
+            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+            "algorithmic_flop_per_launch": gu_fl, "ms_per_launch": gu_ms}
+    clocks = sampler.summary(min(main_res["t0"], dec["t0"]), max(main_res["t1"], dec["t1"]))
+
+    dms = dec["ms"]
+    dst = dec["stages"]
+    d_gu_ms = float(dst[names.index("gateup_gemm")])
+    d_dn_ms = float(dst[names.index("down_gemm")])
+    d_gu_bytes = gateup_weight_bytes(dc, dec["counts"])
+    decode = {"workload": workload_config(dc)["workload"], "value": dc["T"] * world / (dms * 1e-3),
+              "unit": "tokens/s", "ms_per_step": dms, "layer": dec["layer"],
+              "stages_ms": {n: float(v) for n, v in zip(names, dst)},
+              "roofline": {"kernel": "gemm_tc_kernel<gate/up+SwiGLU> (tcgen05)", "bound": "hbm",
+                           "achieved": d_gu_bytes / (d_gu_ms * 1e-3) / 1e9,
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": d_gu_bytes / (d_gu_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "traffic": traffic_record("gemm_gateup_decode"),
+                           "peak_source": f"{peak_src} HBM copy"},
+              "experts_touched": int((dec["counts"] > 0).sum())}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        n = CPU_SAMPLE[args.config]
+        v, dt = cpu_oracle_sample(c, main_res["dev"], n)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n} tokens of the {c['name']} batch: router, top-k, routed and "
+                         f"shared experts, combine in fp64 ({dt:.1f} s)"}
+    line = {
+        "metric": "MoE-layer tokens/s, DeepSeek-V3 shape (T=8192 prefill; T=128 decode under "
+                  "'decode')",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(c),
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": int(r_launches(c) * args.steps),
+        "clocks": clocks,
+        "layer": main_res["layer"],
+        "stages_ms": {n: float(v) for n, v in zip(names, st)},
+        "decode": decode,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_profile(args, c):
+    """Warm-up + timed steps of one workload, nothing else (keeps ncu captures small)."""
+    import torch
+    import mixture_experts_layer_83_b300 as moe
+    moe.lib()
+    dev = rank_inputs(c, 0)
+    torch.cuda.synchronize()
+    r = Runner(c, dev)
+    ms, stages, _ = r.timed(args.steps, args.warmup, 1)
+    print(json.dumps({"profile": c["name"], "ms_per_step": ms,
+                      "stages_ms": {n: float(v) for n, v in zip(moe.STAGE_NAMES, stages)}}))
+    return 0
+
+
+def r_launches(c):
+    import mixture_experts_layer_83_b300 as moe
+    dt = moe.MOE_DTYPE_BF16 if c["dtype"] == "bf16" else moe.MOE_DTYPE_F32
+    return moe.moe_layer_num_launches(moe.make_shape(c["T"], c["d"], c["E"], c["k"], c["F"],
+                                                     c["Fs"], dt))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -139,6 +139,9 @@ def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, sha
     if stage_events is None:
         rc = lib().moe_layer_forward(*args)
     else:
+        for e in stage_events:
+            if not e.cuda_event:   # torch creates the CUDA event on its first record
+                e.record()
         arr = (ctypes.c_void_p * MOE_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
         rc = lib().moe_layer_forward_ex(*args, ctypes.byref(MoeForwardOpts(arr)))
     if check and rc != MOE_OK:

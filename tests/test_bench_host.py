@@ -1,0 +1,62 @@
+"""Host logic of bench.py: the max-over-ranks timing reduction with two gloo ranks on CPU,
+and the algorithmic FLOP / byte models against the layer definition."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from moe_inputs import configs
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w, r, _ = bench.dist_info()
+    bench.barrier(w)
+    got = bench.max_over_ranks(10.0 + 5.0 * r, w)
+    q.put((r, w, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert res == [(0, 2, 15.0), (1, 2, 15.0)]
+
+
+def test_flop_model_matches_definition():
+    c = configs.CONFIGS[2]
+    T, d, E, k, F, Fs = 8192, 7168, 256, 8, 2048, 2048
+    assert bench.layer_flops(c) == T * (2 * d * E + k * 3 * 2 * d * F + 3 * 2 * d * Fs)
+    assert abs(bench.layer_flops(c) / 1e12 - 6.524) < 0.001
+    assert bench.gateup_flops(c) == 2 * d * (T * k + T) * 2 * F
+
+
+def test_byte_model_counts_only_touched_experts():
+    c = configs.CONFIGS[3]
+    counts = np.zeros(256, dtype=np.int32)
+    counts[:10] = 1
+    s = 2
+    want = 2 * 128 * 7168 * s + 256 * 7168 * s + 10 * 3 * 7168 * 2048 * s + 3 * 7168 * 2048 * s
+    assert bench.layer_bytes(c, counts) == want
