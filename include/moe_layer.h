@@ -145,8 +145,9 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
  * (host array [E]; ignored for the router) on a device with num_sms SMs.  Writes up to
  * max_tiles rows of 7 ints {operand set (0 routed / 1 shared), segment, weight tile m, first
  * token row, MMA N, rows that belong to the segment, loads second 64-row weight box} into
- * tiles (host), and 8 ints {n-tile cap, pipeline stages, stage bytes, shared-memory bytes,
- * m-tiles of set 0, m-tiles of set 1, m-group, K of set 0} into geometry (host, may be NULL).
+ * tiles (host), and 8 ints {n-tile cap, weight-ring stages, token-ring stages, shared-memory
+ * bytes, m-tiles of set 0, m-tiles of set 1, m-group, K of set 0} into geometry (host, may be
+ * NULL).
  * Returns the schedule's tile count (may exceed max_tiles) or a negative MOE_ERR_*. */
 int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,
                          int* tiles, int max_tiles, int* geometry);

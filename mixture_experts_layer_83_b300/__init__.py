@@ -181,7 +181,7 @@ def moe_debug_gemm_tiles(shape, which, expert_counts=None, num_sms=148):
     lib().moe_debug_gemm_tiles(ctypes.byref(shape), which, num_sms,
                                None if counts is None else counts.ctypes.data, tiles.ctypes.data,
                                n, geo.ctypes.data)
-    keys = ("bn", "stages", "stage_bytes", "smem_bytes", "m_tiles0", "m_tiles1", "group", "K0")
+    keys = ("bn", "stages_a", "stages_b", "smem_bytes", "m_tiles0", "m_tiles1", "group", "K0")
     return tiles[:n], dict(zip(keys, (int(v) for v in geo)))
 
 

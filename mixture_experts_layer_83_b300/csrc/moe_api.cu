@@ -152,7 +152,7 @@ void geometry_router(const moe_shape& s, int sms, TcParams& p) {
   P.nt = (s.T + p.bn - 1) / p.bn;
   P.out_ld = s.E;
   P.out_valid_m = s.E;
-  p.stages = gemm_tc_plan_stages(p.bn, 0, &p.stage_bytes);
+  gemm_tc_plan(p.bn, 0, p);
 }
 
 void geometry_gateup(const moe_shape& s, TcParams& p) {
@@ -187,7 +187,7 @@ void geometry_gateup(const moe_shape& s, TcParams& p) {
     Q.out_ld = s.Fs;
     Q.out_valid_m = INT_MAX;
   }
-  p.stages = gemm_tc_plan_stages(bn, s.E, &p.stage_bytes);
+  gemm_tc_plan(bn, s.E, p);
 }
 
 void geometry_down(const moe_shape& s, TcParams& p) {
@@ -223,7 +223,7 @@ void geometry_down(const moe_shape& s, TcParams& p) {
     Q.out_row_base = s.T * s.k;
     Q.out_valid_m = s.d;
   }
-  p.stages = gemm_tc_plan_stages(bn, s.E, &p.stage_bytes);
+  gemm_tc_plan(bn, s.E, p);
 }
 
 // Geometry plus operand pointers and tensor maps.
@@ -336,7 +336,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   int bn = expert_bn(S);
   if (bf16) {
     if (plan_bf16(S, x, w_router, w_gate_up, w_down, sh, ws, L, sms, pl) != 0) return MOE_ERR_CUDA;
-    if (pl.router.stages < 2 || pl.gateup.stages < 2 || pl.down.stages < 2) return MOE_ERR_UNSUPPORTED;
+    if (pl.router.stages_a < 2 || pl.gateup.stages_a < 2 || pl.down.stages_a < 2) return MOE_ERR_UNSUPPORTED;
   }
   cudaEvent_t* ev = opts ? opts->stage_events : nullptr;
   auto mark = [&](int i) -> bool { return ev == nullptr || cudaEventRecord(ev[i], stream) == cudaSuccess; };
@@ -500,8 +500,8 @@ int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* 
   }
   if (geometry) {
     geometry[0] = p.bn;
-    geometry[1] = p.stages;
-    geometry[2] = p.stage_bytes;
+    geometry[1] = p.stages_a;
+    geometry[2] = p.stages_b;
     geometry[3] = (int)gemm_tc_smem_bytes(p);
     geometry[4] = p.prob[0].m_tiles;
     geometry[5] = p.n_prob > 1 ? p.prob[1].m_tiles : 0;

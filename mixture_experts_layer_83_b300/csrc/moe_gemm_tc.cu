@@ -8,10 +8,15 @@
 // segments.  The experts run as one grouped GEMM over the expert segments (page "Tensor vs
 // Expert vs Data Parallelism for MoE Serving", Figure 2: experts run grouped GEMMs).
 //
-// Roles (192 threads, one CTA per SM, persistent over a static tile stride):
-//   warp 0 lane 0   TMA producer: weight boxes + token boxes into an smem ring (S stages)
-//   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma (K=16) per stage into one of two TMEM
-//                   accumulators (256 columns each), commits release stages / accumulators
+// Roles (224 threads, one CTA per SM, persistent over a static tile stride):
+//   warp 0 lane 0   weight producer: TMA of the 128 x 64 weight block of each k-step into
+//                   the weight ring (16 KiB stages, up to 12 deep): weights come from HBM
+//                   and need the longest look-ahead
+//   warp 6 lane 0   token producer: TMA of the N x 64 token block into the token ring (a few
+//                   stages: token tiles are L2 hits, re-read by every weight tile)
+//   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma (K=16) per k-step into one of two TMEM
+//                   accumulators (256 columns each); commits release ring stages and hand
+//                   finished accumulators to the epilogue
 //   warps 2..5      epilogue: tcgen05.ld, then per mode
 //                     router : fp32 logits [T][E]
 //                     gate/up: rows 0..63 of A are gate rows, 64..127 the matching up rows;
@@ -19,7 +24,7 @@
 //                              own the two halves through shared memory, stored as bf16
 //                     down   : y rows (bf16)
 // The tile scheduler reads the segment offsets and the n-tile prefix the dispatch scan wrote,
-// so nothing crosses to the host.  Tile order within a segment is (m-group, n-tile, m), so the
+// so nothing crosses to the host.  Tile order within a segment is (m-group, m, n-tile), so the
 // CTAs running at the same time share weight tiles (all n-tiles of an m) and token tiles (a
 // group of m) through L2.
 #include <cuda.h>
@@ -36,14 +41,15 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kMaxStages = 8;
+constexpr int kThreads = 224;
+constexpr int kMaxStagesA = 12;
+constexpr int kMaxStagesB = 4;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
-constexpr int kABytes = 128 * 128;       // 128 rows x 64 bf16
+constexpr int kABytes = 128 * 128;       // weight stage: 128 rows x 64 bf16
 constexpr int kXchgLd = 17;              // padded row of the gate/up exchange buffers
 constexpr int kXchgFloats = 2 * 2 * 32 * kXchgLd;
-constexpr int kBarBytes = 256;           // 21 mbarriers, rounded
+constexpr int kBarBytes = 512;           // 2 * (12 + 4) + 5 mbarriers, rounded
 constexpr int kMiscBytes = 128;
 constexpr size_t kSmemLimit = 232448;    // 227 KiB opt-in per CTA
 constexpr size_t kSmemFloor = 120 * 1024;  // keeps a second CTA (and TMEM demand) off the SM
@@ -56,17 +62,27 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Wait for every load a producer armed on its ring (used when unwinding after an abort).
+__device__ void drain_ring(uint64_t* full, const int* armed, int stages, int* err) {
+  for (int s = 0; s < stages; ++s)
+    if (armed[s] > 0 && !drain_wait(&full[s], static_cast<uint32_t>(armed[s] - 1) & 1u))
+      atomicCAS(err, 0, kErrDrainWait);
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int S = p.stages;
-  uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kMaxStages;
-  uint64_t* tfull = bars + 2 * kMaxStages;
+  const int SA = p.stages_a, SB = p.stages_b;
+  uint8_t* ring_a = smem;
+  uint8_t* ring_b = smem + (size_t)SA * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_b + (size_t)SB * p.b_stage_bytes);
+  uint64_t* full_a = bars;
+  uint64_t* empty_a = full_a + kMaxStagesA;
+  uint64_t* full_b = empty_a + kMaxStagesA;
+  uint64_t* empty_b = full_b + kMaxStagesB;
+  uint64_t* tfull = empty_b + kMaxStagesB;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   int* misc = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
@@ -79,9 +95,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&full_a[s], 1);
+      mbar_init(&empty_a[s], 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&full_b[s], 1);
+      mbar_init(&empty_b[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -117,108 +137,141 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   const int total = tiles0 + tiles1;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- weight producer
     if (lane == 0) {
-    const uint64_t pol_w = l2_policy_evict_first();
-    const uint64_t pol_x = l2_policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    int armed[kMaxStages];
-    for (int s = 0; s < kMaxStages; ++s) armed[s] = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      Tile tl;
-      decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
-      const TcProblem& P = p.prob[tl.prob];
-      const int arow = tl.seg * P.a_seg_stride + tl.m * P.a_m_stride;
-      const bool box1 = tile_has_box1(P, tl);
-      const uint32_t bytes =
-          static_cast<uint32_t>((box1 ? 2 : 1) * P.a_box_rows * 128 + tl.ncols * 128);
-      const int kblocks = P.K >> 6;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
-          ok = false;
-          break;
-        }
-        uint8_t* sA = stages + (size_t)stage * p.stage_bytes;
-        uint8_t* sB = sA + kABytes;
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        ++armed[stage];
-        const int kx = kb * 64;
-        tma_load_2d(sA, &P.tmA, &full[stage], kx, arow, pol_w);
-        if (box1) tma_load_2d(sA + 64 * 128, &P.tmA, &full[stage], kx, arow + P.a_box1_off, pol_w);
-        int off = 0, rem = tl.ncols;
-        while (rem >= 128) {
-          tma_load_2d(sB + off * 128, &P.tmB[0], &full[stage], kx, tl.row0 + off, pol_x);
-          off += 128;
-          rem -= 128;
-        }
-        if (rem & 64) {
-          tma_load_2d(sB + off * 128, &P.tmB[1], &full[stage], kx, tl.row0 + off, pol_x);
-          off += 64;
-        }
-        if (rem & 32) {
-          tma_load_2d(sB + off * 128, &P.tmB[2], &full[stage], kx, tl.row0 + off, pol_x);
-          off += 32;
-        }
-        if (rem & 16) tma_load_2d(sB + off * 128, &P.tmB[3], &full[stage], kx, tl.row0 + off, pol_x);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
+      // weights read by one tile only stream through L2 (evict first); weights a neighbouring
+      // n-tile reads again stay at normal priority
+      const uint64_t pol_once = l2_policy_evict_first();
+      const uint64_t pol_shared = l2_policy_evict_normal();
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[kMaxStagesA];
+      for (int s = 0; s < kMaxStagesA; ++s) armed[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
+        const TcProblem& P = p.prob[tl.prob];
+        const int arow = tl.seg * P.a_seg_stride + tl.m * P.a_m_stride;
+        const bool box1 = tile_has_box1(P, tl);
+        const uint64_t pol = tl.nt > 1 ? pol_shared : pol_once;
+        const uint32_t bytes = static_cast<uint32_t>((box1 ? 2 : 1) * P.a_box_rows * 128);
+        const int kblocks = P.K >> 6;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty_a[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = ring_a + (size_t)stage * kABytes;
+          mbar_arrive_expect_tx(&full_a[stage], bytes);
+          ++armed[stage];
+          tma_load_2d(sA, &P.tmA, &full_a[stage], kb * 64, arow, pol);
+          if (box1) tma_load_2d(sA + 64 * 128, &P.tmA, &full_a[stage], kb * 64, arow + P.a_box1_off, pol);
+          if (++stage == SA) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
+      if (!ok) drain_ring(full_a, armed, SA, p.err);
     }
-    if (!ok) {
-      // copies still in flight must land before the CTA's shared memory goes away
-      for (int s = 0; s < S; ++s)
-        if (armed[s] > 0 && !drain_wait(&full[s], static_cast<uint32_t>(armed[s] - 1) & 1u))
-          atomicCAS(p.err, 0, kErrDrainWait);
-    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ---------------------------------------------------------------- token producer
+    if (lane == 0) {
+      const uint64_t pol_x = l2_policy_evict_last();  // re-read by every weight tile
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[kMaxStagesB];
+      for (int s = 0; s < kMaxStagesB; ++s) armed[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
+        const TcProblem& P = p.prob[tl.prob];
+        const uint32_t bytes = static_cast<uint32_t>(tl.ncols * 128);
+        const int kblocks = P.K >> 6;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty_b[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sB = ring_b + (size_t)stage * p.b_stage_bytes;
+          mbar_arrive_expect_tx(&full_b[stage], bytes);
+          ++armed[stage];
+          const int kx = kb * 64;
+          int off = 0, rem = tl.ncols;
+          while (rem >= 128) {
+            tma_load_2d(sB + off * 128, &P.tmB[0], &full_b[stage], kx, tl.row0 + off, pol_x);
+            off += 128;
+            rem -= 128;
+          }
+          if (rem & 64) {
+            tma_load_2d(sB + off * 128, &P.tmB[1], &full_b[stage], kx, tl.row0 + off, pol_x);
+            off += 64;
+          }
+          if (rem & 32) {
+            tma_load_2d(sB + off * 128, &P.tmB[2], &full_b[stage], kx, tl.row0 + off, pol_x);
+            off += 32;
+          }
+          if (rem & 16) tma_load_2d(sB + off * 128, &P.tmB[3], &full_b[stage], kx, tl.row0 + off, pol_x);
+          if (++stage == SB) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) drain_ring(full_b, armed, SB, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc_i = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      Tile tl;
-      decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
-      const TcProblem& P = p.prob[tl.prob];
-      const int buf = acc_i & 1;
-      const uint32_t use = static_cast<uint32_t>(acc_i >> 1);
-      if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait)) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccCols);
-      const uint32_t idesc = idesc_bf16_f32(128, tl.ncols);
-      const int kblocks = P.K >> 6;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMmaWait)) {
-          ok = false;
-          break;
-        }
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
+      int acc_i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile tl;
+        decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
+        const TcProblem& P = p.prob[tl.prob];
+        const int buf = acc_i & 1;
+        const uint32_t use = static_cast<uint32_t>(acc_i >> 1);
+        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(stages + (size_t)stage * p.stage_bytes);
-        const uint64_t ad = sdesc_k_sw128(a0);
-        const uint64_t bd = sdesc_k_sw128(a0 + kABytes);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccCols);
+        const uint32_t idesc = idesc_bf16_f32(128, tl.ncols);
+        const int kblocks = P.K >> 6;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full_a[sa], pa, abort_flag, p.err, kErrMmaWait) ||
+              !mbar_wait(&full_b[sb], pb, abort_flag, p.err, kErrMmaWait)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)sa * kABytes));
+          const uint64_t bd = sdesc_k_sw128(smem_u32(ring_b + (size_t)sb * p.b_stage_bytes));
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
-        mma_commit(&empty[stage]);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
+          for (int j = 0; j < 4; ++j)
+            mma_bf16(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
+          mma_commit(&empty_a[sa]);
+          mma_commit(&empty_b[sb]);
+          if (++sa == SA) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sb == SB) {
+            sb = 0;
+            pb ^= 1u;
+          }
         }
+        if (!ok) break;
+        mma_commit(&tfull[buf]);
+        ++acc_i;
       }
-      if (!ok) break;
-      mma_commit(&tfull[buf]);
-      ++acc_i;
-    }
-    // every MMA this thread issued completes before tensor memory is released
-    mma_commit(drain);
-    if (!drain_wait(drain, 0)) atomicCAS(p.err, 0, kErrDrainWait);
+      // every MMA this thread issued completes before tensor memory is released
+      mma_commit(drain);
+      if (!drain_wait(drain, 0)) atomicCAS(p.err, 0, kErrDrainWait);
     }
     __syncwarp();
   } else {
@@ -358,18 +411,20 @@ cudaError_t launch_mode(const TcParams& p, int grid, size_t smem, cudaStream_t s
 
 }  // namespace
 
-int gemm_tc_plan_stages(int bn, int n_seg, int* stage_bytes) {
-  const int sb = kABytes + bn * 128;
-  const size_t avail = kSmemLimit - fixed_smem_bytes(n_seg);
-  int st = static_cast<int>(avail / sb);
-  if (st > kMaxStages) st = kMaxStages;
-  *stage_bytes = sb;
-  return st;
+// Ring depths for an n-tile cap: the token ring holds a few stages (its loads hit L2), the
+// weight ring takes the rest of shared memory (its loads come from HBM).
+void gemm_tc_plan(int bn, int n_seg, TcParams& p) {
+  p.b_stage_bytes = bn * 128;
+  p.stages_b = bn >= 128 ? 3 : 4;
+  const size_t avail = kSmemLimit - fixed_smem_bytes(n_seg) - (size_t)p.stages_b * p.b_stage_bytes;
+  int sa = static_cast<int>(avail / kABytes);
+  p.stages_a = sa > kMaxStagesA ? kMaxStagesA : sa;
 }
 
 size_t gemm_tc_smem_bytes(const TcParams& p) {
   const int n_seg = p.prob[0].seg_off != nullptr ? p.prob[0].n_seg : 0;
-  size_t b = fixed_smem_bytes(n_seg) + (size_t)p.stages * p.stage_bytes;
+  size_t b = fixed_smem_bytes(n_seg) + (size_t)p.stages_a * kABytes +
+             (size_t)p.stages_b * p.b_stage_bytes;
   return b < kSmemFloor ? kSmemFloor : b;
 }
 
@@ -389,7 +444,9 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 
 cudaError_t launch_gemm_tc(int mode, const TcParams& p, int grid, cudaStream_t s) {
   const size_t smem = gemm_tc_smem_bytes(p);
-  if (smem > kSmemLimit || p.stages < 2) return cudaErrorInvalidConfiguration;
+  if (smem > kSmemLimit || p.stages_a < 2 || p.stages_b < 2 || p.stages_a > kMaxStagesA ||
+      p.stages_b > kMaxStagesB)
+    return cudaErrorInvalidConfiguration;
   switch (mode) {
     case kModeRouter: return launch_mode<kModeRouter>(p, grid, smem, s);
     case kModeGateUp: return launch_mode<kModeGateUp>(p, grid, smem, s);

@@ -52,15 +52,16 @@ struct TcProblem {
 struct TcParams {
   TcProblem prob[2];
   int n_prob;
-  int bn;           // n-tile cap: multiple of 16, at most 256
-  int stages;       // smem pipeline depth
-  int stage_bytes;  // 16 KiB A + bn * 128 B B
-  int* err;         // device status word
+  int bn;             // n-tile cap: multiple of 16, at most 256
+  int stages_a;       // depth of the weight ring (16 KiB stages)
+  int stages_b;       // depth of the token ring
+  int b_stage_bytes;  // bn * 128 B
+  int* err;           // device status word
 };
 
 // Tensor-core GEMM (moe_gemm_tc.cu).
 size_t gemm_tc_smem_bytes(const TcParams& p);
-int gemm_tc_plan_stages(int bn, int n_seg, int* stage_bytes);
+void gemm_tc_plan(int bn, int n_seg, TcParams& p);
 cudaError_t launch_gemm_tc(int mode, const TcParams& p, int grid, cudaStream_t s);
 int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);

@@ -19,12 +19,15 @@ struct Tile {
   int row0;   // first B row of the tile
   int ncols;  // MMA N: multiple of 16, at most the n-tile cap
   int valid;  // B rows of the tile that belong to the segment (<= ncols)
+  int nt;     // n-tiles of the segment (> 1: the weight tile is read again by a neighbour)
 };
 
 // Tile t of the schedule.  Operand set 0 comes first (tiles0 tiles), then set 1.  Within a
-// segment tiles run in (m-group, n-tile, m) order.  A segment of n rows is cut into nt n-tiles
-// of whole 16-row units, as even as possible.  `seg` / `ntp` are the segment row offsets and
-// the n-tile prefix of set 0 when it is grouped.
+// segment tiles run in (m-group, m, n-tile) order: the n-tiles that share a weight tile are
+// neighbours in the schedule (and so run at the same time on neighbouring CTAs, sharing the
+// weight tile through L2), and a group of m-tiles shares each token tile.  A segment of n
+// rows is cut into nt n-tiles of whole 16-row units, as even as possible.  `seg_off` / `ntp`
+// are the segment row offsets and the n-tile prefix of set 0 when it is grouped.
 MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, int tiles0, int t,
                         Tile& tl) {
   int prob = 0, local = t;
@@ -55,10 +58,12 @@ MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, i
   const int G = P.group;
   const int mg = local / (G * nt);
   const int r = local - mg * G * nt;
-  const int j = r / G;
+  const int mi = r / nt;
+  const int j = r - mi * nt;
   tl.prob = prob;
   tl.seg = seg;
-  tl.m = mg * G + (r - j * G);
+  tl.m = mg * G + mi;
+  tl.nt = nt;
   const int units = (seg_rows + 15) >> 4;
   const int q16 = units / nt, rem = units - q16 * nt;
   const int u0 = j * q16 + (j < rem ? j : rem);
