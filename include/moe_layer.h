@@ -140,6 +140,23 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
                         int* sorted_token, int* slot_pos, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_route_from_keys for callers that cannot allocate device memory (an allocator they do
+ * not own, a pool that is already carved up, a C host with no allocator wired in).  The
+ * pages have no counterpart: this is a convenience of this library.  Same arguments and
+ * results as moe_route_from_keys without the workspace: the dispatch histogram lives in a
+ * fixed array of MOE_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that loads
+ * the library until the process exits.  Shapes whose histogram ((T*k + 1023)/1024 chunks x E
+ * int32) does not fit are rejected with MOE_ERR_WORKSPACE before anything is enqueued.
+ * The first call on a device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.  Every call on a device shares
+ * the array, so calls whose work overlaps on the GPU race and must be serialised by the
+ * caller.  No memory is allocated or freed. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+int moe_route_from_keys_noalloc(const moe_shape* s, const float* sel_key,
+                                const float* gate_score, int* topk_idx, float* topk_w,
+                                int* expert_counts, int* expert_offsets, int* sorted_token,
+                                int* slot_pos, cudaStream_t stream);
+
 /* Diagnostics, host only (launches nothing): the tile schedule the bf16 grouped GEMM `which`
  * (0 = router, 1 = gate/up, 2 = down) would run for the given per-expert token counts
  * (host array [E]; ignored for the router) on a device with num_sms SMs.  Writes up to

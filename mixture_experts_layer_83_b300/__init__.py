@@ -26,8 +26,9 @@ MOE_NUM_STAGE_EVENTS = 8
 STAGE_NAMES = ("router_gemm", "topk", "dispatch", "gather", "gateup_gemm", "down_gemm", "combine")
 
 EXPORTED = ("moe_layer_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
-            "moe_route_from_keys", "moe_debug_gemm_tiles", "moe_layer_num_launches",
-            "moe_workspace_status", "moe_status_string")
+            "moe_route_from_keys", "moe_route_from_keys_noalloc", "moe_debug_gemm_tiles",
+            "moe_layer_num_launches", "moe_workspace_status", "moe_status_string")
+MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class MoeShape(ctypes.Structure):
@@ -72,6 +73,8 @@ def lib():
         l.moe_layer_forward_ex.restype = ci
         l.moe_route_from_keys.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         l.moe_route_from_keys.restype = ci
+        l.moe_route_from_keys_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        l.moe_route_from_keys_noalloc.restype = ci
         l.moe_debug_gemm_tiles.argtypes = [shp, ci, ci, vp, vp, ci, vp]
         l.moe_debug_gemm_tiles.restype = ci
         l.moe_layer_num_launches.argtypes = [shp]
@@ -163,6 +166,19 @@ def moe_route_from_keys(shape, sel_key, gate_score, topk_idx, topk_w, expert_cou
                                    _ptr(workspace), int(workspace_bytes), _stream(stream))
     if check and rc != MOE_OK:
         raise MoeError(rc, "moe_route_from_keys")
+    return rc
+
+
+def moe_route_from_keys_noalloc(shape, sel_key, gate_score, topk_idx, topk_w, expert_counts,
+                                expert_offsets, sorted_token, slot_pos, stream=None, check=True):
+    """moe_route_from_keys without a workspace, for callers that cannot allocate device memory:
+    the scratch is a fixed array inside the library (see include/moe_layer.h)."""
+    rc = lib().moe_route_from_keys_noalloc(ctypes.byref(shape), _ptr(sel_key), _ptr(gate_score),
+                                           _ptr(topk_idx), _ptr(topk_w), _ptr(expert_counts),
+                                           _ptr(expert_offsets), _ptr(sorted_token),
+                                           _ptr(slot_pos), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoeError(rc, "moe_route_from_keys_noalloc")
     return rc
 
 
