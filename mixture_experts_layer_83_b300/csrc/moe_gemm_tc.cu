@@ -20,9 +20,10 @@
 //   warps 2..5      epilogue: tcgen05.ld, then per mode
 //                     router : fp32 logits [T][E]
 //                     gate/up: rows 0..63 of A are gate rows, 64..127 the matching up rows;
-//                              h = silu(gate) * up, exchanged between the warp pairs that
-//                              own the two halves through shared memory, stored as bf16
-//                     down   : y rows (bf16)
+//                              both are staged token-major in shared memory, then each thread
+//                              forms h = silu(gate) * up for 8 features of one token and
+//                              stores them as one 16-byte bf16 vector
+//                     down   : y staged token-major (bf16), stored as full 16-byte rows
 // The tile scheduler reads the segment offsets and the n-tile prefix the dispatch scan wrote,
 // so nothing crosses to the host.  Tile order within a segment is (m-group, m, n-tile), so the
 // CTAs running at the same time share weight tiles (all n-tiles of an m) and token tiles (a
@@ -47,8 +48,10 @@ constexpr int kMaxStagesB = 4;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
 constexpr int kABytes = 128 * 128;       // weight stage: 128 rows x 64 bf16
-constexpr int kXchgLd = 17;              // padded row of the gate/up exchange buffers
-constexpr int kXchgFloats = 2 * 2 * 32 * kXchgLd;
+constexpr int kStageLdF = 68;            // fp32 row of the gate/up staging (64 + pad)
+constexpr int kStageLdH = 136;           // bf16 row of the down staging (128 + pad)
+constexpr int kXchgFloats = 2 * 16 * kStageLdF;  // 8704 B, also holds 32 x kStageLdH bf16
+static_assert(32 * kStageLdH * 2 <= kXchgFloats * 4, "down staging fits the epilogue buffer");
 constexpr int kBarBytes = 512;           // 2 * (12 + 4) + 5 mbarriers, rounded
 constexpr int kMiscBytes = 128;
 constexpr size_t kSmemLimit = 232448;    // 227 KiB opt-in per CTA
@@ -291,51 +294,74 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kAccCols);
       const int nchunks = (tl.valid + 31) >> 5;
+      const int ep = threadIdx.x - 64;  // 0..127 across the four epilogue warps
       if (MODE == kModeGateUp) {
-        const int pair = q & 1;
-        const bool up = q >= 2;
-        float* xg = xchg + pair * (2 * 32 * kXchgLd);  // gate values handed to the up warp
-        float* xu = xg + 32 * kXchgLd;                 // up values handed to the gate warp
-        const int f = tl.m * 64 + pair * 32 + lane;
+        // Rows 0..63 of the accumulator are gate features, 64..127 the matching up features.
+        // Per 16 tokens: every warp stages its 32 features x 16 tokens (fp32) token-major in
+        // shared memory, then each thread computes 8 consecutive h features of one token and
+        // stores them as one 16-byte vector (a warp writes four full 128-byte h rows).
+        float* gs = xchg;                // [16 tokens][kStageLdF] gate
+        float* us = xchg + 16 * kStageLdF;  // [16 tokens][kStageLdF] up
+        float* mine = q < 2 ? gs : us;
+        const int fl = (q & 1) * 32 + lane;  // this lane's feature within the tile's 64
+        const int tt = ep >> 3, fg = ep & 7;
         __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(P.out);
         for (int c = 0; c < nchunks; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), v);
-          if (!up) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xg[lane * kXchgLd + j] = __uint_as_float(v[16 + j]);
-          } else {
+          for (int half = 0; half < 2; ++half) {
+            const int col0 = c * 32 + half * 16;
+            if (col0 >= tl.valid) break;  // uniform over the 128 epilogue threads
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xu[lane * kXchgLd + j] = __uint_as_float(v[j]);
-          }
-          named_bar_sync(2 + pair, 64);
-          const int col0 = c * 32 + (up ? 16 : 0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g = up ? xg[lane * kXchgLd + j] : __uint_as_float(v[j]);
-            const float u = up ? __uint_as_float(v[16 + j]) : xu[lane * kXchgLd + j];
-            const int col = col0 + j;
+            for (int j = 0; j < 16; ++j) mine[j * kStageLdF + fl] = __uint_as_float(v[half * 16 + j]);
+            named_bar_sync(2, 128);
+            const int col = col0 + tt;
             if (col < tl.valid) {
-              const float hv = g / (1.f + __expf(-g)) * u;
-              hout[(size_t)(P.out_row_base + tl.row0 + col) * P.out_ld + f] = __float2bfloat16_rn(hv);
+              const float4* g4 = reinterpret_cast<const float4*>(gs + tt * kStageLdF + fg * 8);
+              const float4* u4 = reinterpret_cast<const float4*>(us + tt * kStageLdF + fg * 8);
+              const float4 ga = g4[0], gb = g4[1], ua = u4[0], ub = u4[1];
+              const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+              const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+              uint4 o;
+              __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float h0 = __fdividef(g[2 * i] * u[2 * i], 1.f + __expf(-g[2 * i]));
+                const float h1 =
+                    __fdividef(g[2 * i + 1] * u[2 * i + 1], 1.f + __expf(-g[2 * i + 1]));
+                oh[i] = __floats2bfloat162_rn(h0, h1);
+              }
+              *reinterpret_cast<uint4*>(hout + (size_t)(P.out_row_base + tl.row0 + col) * P.out_ld +
+                                        tl.m * 64 + fg * 8) = o;
             }
+            named_bar_sync(2, 128);
           }
-          named_bar_sync(2 + pair, 64);
         }
       } else if (MODE == kModeDown) {
-        const int ch = tl.m * 128 + q * 32 + lane;
-        const bool ch_ok = ch < P.out_valid_m;
+        // Per 32 tokens: each lane writes its channel's 32 values (bf16) token-major into
+        // shared memory; then the 128 threads store full 256-byte y rows in 16-byte vectors.
+        __nv_bfloat16* ys = reinterpret_cast<__nv_bfloat16*>(xchg);  // [32][kStageLdH]
+        const int chl = q * 32 + lane;
         __nv_bfloat16* yout = static_cast<__nv_bfloat16*>(P.out);
         for (int c = 0; c < nchunks; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = c * 32 + j;
-            if (ch_ok && col < tl.valid)
-              yout[(size_t)(P.out_row_base + tl.row0 + col) * P.out_ld + ch] =
-                  __float2bfloat16_rn(__uint_as_float(v[j]));
+          for (int j = 0; j < 32; ++j) ys[j * kStageLdH + chl] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          named_bar_sync(2, 128);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = i * 128 + ep;
+            const int tok = idx >> 4, part = idx & 15;
+            const int col = c * 32 + tok;
+            const int ch0 = tl.m * 128 + part * 8;
+            if (col < tl.valid && ch0 < P.out_valid_m)
+              *reinterpret_cast<uint4*>(yout + (size_t)(P.out_row_base + tl.row0 + col) * P.out_ld +
+                                        ch0) =
+                  *reinterpret_cast<const uint4*>(ys + tok * kStageLdH + part * 8);
           }
+          named_bar_sync(2, 128);
         }
       } else {
         const int e = tl.m * 128 + q * 32 + lane;

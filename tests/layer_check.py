@@ -153,3 +153,78 @@ def full_check(cfg, dev=None, host=None, threads=None):
     stats = check_output(c, res["out"], ref)
     stats["excluded"] = n_ex
     return stats
+
+
+def _host_elems(t):
+    """Device tensor -> host array in the oracle's element format (bf16 bits / fp32)."""
+    import torch
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
+    """Full-size check: the whole layer runs on the GPU as bench.py runs it; routing is checked
+    for every token, dispatch tables bit-exactly, outputs on a seeded sample of tokens (plus
+    the first token of the hottest and of the coldest non-empty expert).  The oracle evaluates
+    each sampled (token, expert) pair with its SwiGLU and sums them with its combine; expert
+    weights are copied to the host one expert at a time."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    c = configs.get(cfg)
+    threads = threads or max(1, os.cpu_count() or 1)
+    res = to_host(gpu_forward(c, dev))
+    x = _host_elems(dev["x"])
+    wr = _host_elems(dev["w_router"])
+    bias = dev["bias"].cpu().numpy() if "bias" in dev else None
+    key, score, o_idx, margin = oracle_routing(c, x, wr, bias, threads)
+    n_ex, w_ref = check_routing(c, key, score, margin, o_idx, res["topk_idx"], res["topk_w"])
+    counts = check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"])
+    T, k = c["T"], c["k"]
+    if n_sample >= T:
+        sample = np.arange(T)
+    else:
+        rng = np.random.default_rng(seed)
+        sample = set(rng.choice(T, n_sample, replace=False).tolist())
+        idx = res["topk_idx"]
+        hot = int(np.argmax(counts))
+        cold = int(np.argmin(np.where(counts > 0, counts, np.iinfo(np.int32).max)))
+        for e in (hot, cold):
+            sample.add(int(np.where((idx == e).any(1))[0][0]))
+        sample = np.array(sorted(sample))
+    n = sample.size
+    g_idx = res["topk_idx"][sample]
+    xs64 = as_float64(c, x[sample])
+    ys = np.zeros((n * k, c["d"]))
+    by_expert = {}
+    for i in range(n):
+        for j in range(k):
+            by_expert.setdefault(int(g_idx[i, j]), []).append((i, j))
+
+    def run_expert(e):
+        wgu = _host_elems(dev["w_gate_up"][e])
+        wd = _host_elems(dev["w_down"][e])
+        for i, j in by_expert[e]:
+            ys[i * k + j] = oracle.swiglu_ffn(xs64[i], wgu, wd)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run_expert, sorted(by_expert)))
+    y_sh = None
+    if c["Fs"] > 0:
+        shg, shd = _host_elems(dev["sh_gate_up"]), _host_elems(dev["sh_down"])
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            y_sh = np.stack(list(ex.map(lambda i: oracle.swiglu_ffn(xs64[i], shg, shd),
+                                        range(n))))
+    slots = np.arange(n * k, dtype=np.int32).reshape(n, k)
+    ref = oracle.combine(slots, w_ref[sample], ys, y_sh)
+    stats = check_output(c, res["out"][sample], ref)
+    stats.update(excluded=n_ex, sampled=int(n), experts_touched=int((counts > 0).sum()),
+                 max_over_mean=float(counts.max() / counts.mean()))
+    return stats
+
+
+def as_float64(cfg, arr):
+    if arr.dtype == np.uint16:
+        return (arr.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return np.asarray(arr, dtype=np.float64)
