@@ -187,7 +187,7 @@ def moe_debug_gemm_tiles(shape, which, expert_counts=None, num_sms=148):
     (tiles [n][7] int32 numpy array, geometry dict)."""
     import numpy as np
     counts = None if expert_counts is None else np.ascontiguousarray(expert_counts, np.int32)
-    geo = np.zeros(8, dtype=np.int32)
+    geo = np.zeros(9, dtype=np.int32)
     n = lib().moe_debug_gemm_tiles(ctypes.byref(shape), which, num_sms,
                                    None if counts is None else counts.ctypes.data, None, 0,
                                    geo.ctypes.data)
@@ -197,7 +197,8 @@ def moe_debug_gemm_tiles(shape, which, expert_counts=None, num_sms=148):
     lib().moe_debug_gemm_tiles(ctypes.byref(shape), which, num_sms,
                                None if counts is None else counts.ctypes.data, tiles.ctypes.data,
                                n, geo.ctypes.data)
-    keys = ("bn", "stages_a", "stages_b", "smem_bytes", "m_tiles0", "m_tiles1", "group", "K0")
+    keys = ("bn", "stages_a", "stages_b", "smem_bytes", "m_tiles0", "m_tiles1", "group", "K0",
+            "cg")
     return tiles[:n], dict(zip(keys, (int(v) for v in geo)))
 
 

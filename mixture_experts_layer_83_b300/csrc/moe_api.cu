@@ -124,8 +124,8 @@ int router_bn(const moe_shape& s, int sms) {
 }
 
 int encode_tokens(TcProblem& P, const void* base, int rows, int cols) {
-  const uint32_t boxes[4] = {128, 64, 32, 16};
-  for (int b = 0; b < 4; ++b)
+  const uint32_t boxes[5] = {128, 64, 32, 16, 8};
+  for (int b = 0; b < 5; ++b)
     if (encode_tmap_bf16(&P.tmB[b], base, (uint64_t)rows, (uint64_t)cols, boxes[b]) != 0) return -1;
   return 0;
 }
@@ -139,10 +139,12 @@ void geometry_router(const moe_shape& s, int sms, TcParams& p) {
   memset(&p, 0, sizeof(p));
   TcProblem& P = p.prob[0];
   p.n_prob = 1;
+  p.cg = 1;
   p.bn = router_bn(s, sms);
   P.a_box_rows = s.E < 64 ? s.E : 64;
   P.K = s.d;
-  P.m_tiles = (s.E + 127) / 128;
+  P.m_cta = (s.E + 127) / 128;
+  P.m_tiles = P.m_cta;
   P.group = largest_group(P.m_tiles);
   P.a_seg_stride = 0;
   P.a_m_stride = 128;
@@ -155,17 +157,24 @@ void geometry_router(const moe_shape& s, int sms, TcParams& p) {
   gemm_tc_plan(p.bn, 0, p);
 }
 
+// The expert GEMMs run on CTA pairs: a scheduled m-tile is two 128-row weight tiles.
+void set_m_tiles(TcProblem& P, int m_cta, int cg) {
+  P.m_cta = m_cta;
+  P.m_tiles = cg == 2 ? (m_cta + 1) / 2 : m_cta;
+  P.group = largest_group(P.m_tiles);
+}
+
 void geometry_gateup(const moe_shape& s, TcParams& p) {
   memset(&p, 0, sizeof(p));
   const int bn = expert_bn(s);
   p.n_prob = s.Fs > 0 ? 2 : 1;
+  p.cg = 2;
   p.bn = bn;
   TcProblem& P = p.prob[0];
   P.a_box_rows = 64;
   P.n_seg = s.E;
   P.K = s.d;
-  P.m_tiles = s.F / 64;
-  P.group = largest_group(P.m_tiles);
+  set_m_tiles(P, s.F / 64, p.cg);
   P.a_seg_stride = 2 * s.F;
   P.a_m_stride = 64;
   P.a_box1_off = s.F;
@@ -176,8 +185,7 @@ void geometry_gateup(const moe_shape& s, TcParams& p) {
     TcProblem& Q = p.prob[1];
     Q.a_box_rows = 64;
     Q.K = s.d;
-    Q.m_tiles = s.Fs / 64;
-    Q.group = largest_group(Q.m_tiles);
+    set_m_tiles(Q, s.Fs / 64, p.cg);
     Q.a_seg_stride = 0;
     Q.a_m_stride = 64;
     Q.a_box1_off = s.Fs;
@@ -194,13 +202,13 @@ void geometry_down(const moe_shape& s, TcParams& p) {
   memset(&p, 0, sizeof(p));
   const int bn = expert_bn(s);
   p.n_prob = s.Fs > 0 ? 2 : 1;
+  p.cg = 2;
   p.bn = bn;
   TcProblem& P = p.prob[0];
   P.a_box_rows = 64;
   P.n_seg = s.E;
   P.K = s.F;
-  P.m_tiles = (s.d + 127) / 128;
-  P.group = largest_group(P.m_tiles);
+  set_m_tiles(P, (s.d + 127) / 128, p.cg);
   P.a_seg_stride = s.d;
   P.a_m_stride = 128;
   P.a_box1_off = 64;
@@ -211,8 +219,7 @@ void geometry_down(const moe_shape& s, TcParams& p) {
     TcProblem& Q = p.prob[1];
     Q.a_box_rows = 64;
     Q.K = s.Fs;
-    Q.m_tiles = (s.d + 127) / 128;
-    Q.group = largest_group(Q.m_tiles);
+    set_m_tiles(Q, (s.d + 127) / 128, p.cg);
     Q.a_seg_stride = 0;
     Q.a_m_stride = 128;
     Q.a_box1_off = 64;
@@ -486,31 +493,43 @@ int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* 
     tiles0 = p.prob[0].nt * p.prob[0].m_tiles;
   }
   const int total = tiles0 + (p.n_prob > 1 ? p.prob[1].nt * p.prob[1].m_tiles : 0);
-  for (int t = 0; t < total && t < max_tiles; ++t) {
+  // one row per CTA tile: a pair's scheduled tile is two CTA tiles (the second one only when
+  // it is inside the weight rows), exactly as the kernel's epilogue decides
+  int n = 0;
+  for (int t = 0; t < total; ++t) {
     Tile tl;
     decode_tile(p, seg, ntp, tiles0, t, tl);
-    int* o = tiles + 7 * (size_t)t;
-    o[0] = tl.prob;
-    o[1] = tl.seg;
-    o[2] = tl.m;
-    o[3] = tl.row0;
-    o[4] = tl.ncols;
-    o[5] = tl.valid;
-    o[6] = tile_has_box1(p.prob[tl.prob], tl) ? 1 : 0;
+    const TcProblem& P = p.prob[tl.prob];
+    for (int r = 0; r < p.cg; ++r) {
+      const int mc = p.cg == 2 ? 2 * tl.m + r : tl.m;
+      if (mc >= P.m_cta) continue;
+      if (tiles != nullptr && n < max_tiles) {
+        int* o = tiles + 7 * (size_t)n;
+        o[0] = tl.prob;
+        o[1] = tl.seg;
+        o[2] = mc;
+        o[3] = tl.row0;
+        o[4] = tl.ncols;
+        o[5] = tl.valid;
+        o[6] = a_has_box1(P, mc) ? 1 : 0;
+      }
+      ++n;
+    }
   }
   if (geometry) {
     geometry[0] = p.bn;
     geometry[1] = p.stages_a;
     geometry[2] = p.stages_b;
     geometry[3] = (int)gemm_tc_smem_bytes(p);
-    geometry[4] = p.prob[0].m_tiles;
-    geometry[5] = p.n_prob > 1 ? p.prob[1].m_tiles : 0;
+    geometry[4] = p.prob[0].m_cta;
+    geometry[5] = p.n_prob > 1 ? p.prob[1].m_cta : 0;
     geometry[6] = p.prob[0].group;
     geometry[7] = p.prob[0].K;
+    geometry[8] = p.cg;
   }
   delete[] seg;
   delete[] ntp;
-  return total;
+  return n;
 }
 
 int moe_layer_num_launches(const moe_shape* s) {

@@ -1,28 +1,39 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) for sm_103a.
 //
-// Computes D = A * B^T per tile, A = 128 weight rows (the MMA's M), B = up to 256 token rows
-// (the MMA's N, any multiple of 16), K in 64-element blocks; bf16 operands, fp32 accumulation
-// in tensor memory.  Putting the weights on M and the tokens on N ("swap AB") lets a tile
-// follow an expert's token count with 16-row granularity, so a ragged expert segment wastes
-// at most 15 rows -- the same kernel serves 256-row prefill segments and 4-row decode
-// segments.  The experts run as one grouped GEMM over the expert segments (page "Tensor vs
-// Expert vs Data Parallelism for MoE Serving", Figure 2: experts run grouped GEMMs).
+// Computes D = A * B^T per tile, A = weight rows (the MMA's M), B = up to 256 token rows (the
+// MMA's N, any multiple of 16), K in 64-element blocks; bf16 operands, fp32 accumulation in
+// tensor memory.  Putting the weights on M and the tokens on N ("swap AB") lets a tile follow
+// an expert's token count with 16-row granularity, so a ragged expert segment wastes at most
+// 15 rows -- the same kernel serves 256-row prefill segments and 4-row decode segments.  The
+// experts run as one grouped GEMM over the expert segments (page "Tensor vs Expert vs Data
+// Parallelism for MoE Serving", Figure 2: experts run grouped GEMMs).
+//
+// Two forms, chosen by the template argument CG:
+//   CG = 1  one CTA per tile: M = 128 weight rows, the CTA holds all N token rows.
+//   CG = 2  a CTA pair (a 2-CTA cluster on the two SMs of a TPC, tcgen05 cta_group::2) per
+//           tile: M = 256 weight rows, each CTA holds its own 128 weight rows and half of the
+//           N token rows, and each CTA's tensor memory receives its 128 rows x N.  Per SM
+//           this moves a third less operand data per FLOP (16 KB of weights + N/2 x 128 B of
+//           tokens per k-block instead of 16 KB + N x 128 B), which is what the expert GEMMs
+//           of a prefill batch are limited by.  Both CTAs' TMA loads count their bytes on the
+//           even CTA's barriers; its MMA issuer runs the pair and its commits arrive on both
+//           CTAs' barriers (multicast).
 //
 // Roles (224 threads, one CTA per SM, persistent over a static tile stride):
 //   warp 0 lane 0   weight producer: TMA of the 128 x 64 weight block of each k-step into
 //                   the weight ring (16 KiB stages, up to 12 deep): weights come from HBM
 //                   and need the longest look-ahead
-//   warp 6 lane 0   token producer: TMA of the N x 64 token block into the token ring (a few
-//                   stages: token tiles are L2 hits, re-read by every weight tile)
-//   warp 1 lane 0   MMA issuer: 4 x tcgen05.mma (K=16) per k-step into one of two TMEM
-//                   accumulators (256 columns each); commits release ring stages and hand
-//                   finished accumulators to the epilogue
+//   warp 6 lane 0   token producer: TMA of this CTA's N (or N/2) x 64 token block into the
+//                   token ring (token tiles are L2 hits, re-read by every weight tile)
+//   warp 1 lane 0   MMA issuer (even CTA of a pair only): 4 x tcgen05.mma (K=16) per k-step
+//                   into one of two TMEM accumulators (256 columns each); commits release ring
+//                   stages and hand finished accumulators to the epilogues
 //   warps 2..5      epilogue: tcgen05.ld, then per mode
 //                     router : fp32 logits [T][E]
-//                     gate/up: rows 0..63 of A are gate rows, 64..127 the matching up rows;
-//                              both are staged token-major in shared memory, then each thread
-//                              forms h = silu(gate) * up for 8 features of one token and
-//                              stores them as one 16-byte bf16 vector
+//                     gate/up: rows 0..63 of the CTA's A are gate rows, 64..127 the matching
+//                              up rows; both are staged token-major in shared memory, then
+//                              each thread forms h = silu(gate) * up for 8 features of one
+//                              token and stores them as one 16-byte bf16 vector
 //                     down   : y staged token-major (bf16), stored as full 16-byte rows
 // The tile scheduler reads the segment offsets and the n-tile prefix the dispatch scan wrote,
 // so nothing crosses to the host.  Tile order within a segment is (m-group, m, n-tile), so the
@@ -44,18 +55,27 @@ namespace {
 
 constexpr int kThreads = 224;
 constexpr int kMaxStagesA = 12;
-constexpr int kMaxStagesB = 4;
-constexpr int kTmemCols = 512;
-constexpr int kAccCols = 256;
+constexpr int kMaxStagesB = 8;
+constexpr int kAccCols = 256;  // one accumulator: 128 lanes x up to 256 fp32 columns
+// One CTA per SM (CG = 1) double-buffers its accumulator in all 512 TMEM columns.  CTA pairs
+// (CG = 2) run two per SM (two pairs per TPC), each with one accumulator of 256 columns: the
+// second pair keeps the tensor cores busy while the first drains its accumulator, and the
+// two MMA issuers per SM halve the per-instruction issue cost that bounds MMAs with N < 256.
+template <int CG> constexpr int acc_bufs() { return CG == 2 ? 1 : 2; }
+template <int CG> constexpr uint32_t tmem_cols() { return static_cast<uint32_t>(acc_bufs<CG>() * kAccCols); }
+template <int CG> constexpr int ctas_per_sm() { return CG == 2 ? 2 : 1; }
 constexpr int kABytes = 128 * 128;       // weight stage: 128 rows x 64 bf16
 constexpr int kStageLdF = 68;            // fp32 row of the gate/up staging (64 + pad)
 constexpr int kStageLdH = 136;           // bf16 row of the down staging (128 + pad)
 constexpr int kXchgFloats = 2 * 16 * kStageLdF;  // 8704 B, also holds 32 x kStageLdH bf16
 static_assert(32 * kStageLdH * 2 <= kXchgFloats * 4, "down staging fits the epilogue buffer");
-constexpr int kBarBytes = 512;           // 2 * (12 + 4) + 5 mbarriers, rounded
+constexpr int kBarBytes = 512;           // 2 * (12 + 8) + 5 mbarriers, rounded
+static_assert(8 * (2 * (kMaxStagesA + kMaxStagesB) + 5) <= kBarBytes, "mbarriers fit");
 constexpr int kMiscBytes = 128;
 constexpr size_t kSmemLimit = 232448;    // 227 KiB opt-in per CTA
-constexpr size_t kSmemFloor = 120 * 1024;  // keeps a second CTA (and TMEM demand) off the SM
+constexpr size_t kSmemLimitPair = 112 * 1024;  // two per SM with room to spare in its 228 KiB
+constexpr size_t kSmemFloor = 120 * 1024;  // keeps a second one-CTA kernel (and its TMEM demand) off the SM
+size_t smem_limit(int cg) { return cg == 2 ? kSmemLimitPair : kSmemLimit; }
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -65,16 +85,34 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-// Wait for every load a producer armed on its ring (used when unwinding after an abort).
+// Wait for every load a producer armed on its ring (used when unwinding after an abort).  One
+// wall-clock limit covers the whole ring.
 __device__ void drain_ring(uint64_t* full, const int* armed, int stages, int* err) {
-  for (int s = 0; s < stages; ++s)
-    if (armed[s] > 0 && !drain_wait(&full[s], static_cast<uint32_t>(armed[s] - 1) & 1u))
-      atomicCAS(err, 0, kErrDrainWait);
+  const uint64_t t0 = globaltimer_ns();
+  for (int s = 0; s < stages; ++s) {
+    if (armed[s] == 0) continue;
+    const uint32_t a = smem_u32(&full[s]);
+    const uint32_t parity = static_cast<uint32_t>(armed[s] - 1) & 1u;
+    while (!mbar_try_wait(a, parity)) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicCAS(err, 0, kErrDrainWait);
+        return;
+      }
+    }
+  }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+template <int MODE, int CG>
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
+  if constexpr (CG == 2) {
+    // a pair kernel launched without 2-CTA clusters: record it and leave before any shared
+    // state exists (the condition is uniform over the grid)
+    if (cluster_nctarank() != 2) {
+      if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrLaunchShape);
+      return;
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int SA = p.stages_a, SB = p.stages_b;
@@ -96,6 +134,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   int* s_ntp = s_seg + (n_seg0 + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // rank within the pair (the even CTA issues the MMAs) and this CTA's stream of tiles
+  const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit0 = CG == 2 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int nunits = CG == 2 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
@@ -108,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 4 * CG);  // one arrival per epilogue warp of each CTA
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -117,12 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   if (threadIdx.x == 32) {
     for (int i = 0; i < p.n_prob; ++i) {
       tma_prefetch_desc(&p.prob[i].tmA);
-      for (int b = 0; b < 4; ++b) tma_prefetch_desc(&p.prob[i].tmB[b]);
+      for (int b = 0; b < 5; ++b) tma_prefetch_desc(&p.prob[i].tmB[b]);
     }
   }
   if (warp == 0) {
-    tmem_alloc(reinterpret_cast<uint32_t*>(misc), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(reinterpret_cast<uint32_t*>(misc), tmem_cols<CG>());
+    tmem_relinquish<CG>();
   }
   if (n_seg0 > 0) {
     for (int i = threadIdx.x; i <= n_seg0; i += kThreads) {
@@ -132,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers are initialised before any remote arrival or TMA completion
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
 
@@ -151,14 +196,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       int armed[kMaxStagesA];
       for (int s = 0; s < kMaxStagesA; ++s) armed[s] = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit0; t < total && ok; t += nunits) {
         Tile tl;
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
-        const int arow = tl.seg * P.a_seg_stride + tl.m * P.a_m_stride;
-        const bool box1 = tile_has_box1(P, tl);
+        const int mc = CG == 2 ? 2 * tl.m + rank : tl.m;
+        const int arow = tl.seg * P.a_seg_stride + mc * P.a_m_stride;
+        const bool box1 = a_has_box1(P, mc);
         const uint64_t pol = tl.nt > 1 ? pol_shared : pol_once;
-        const uint32_t bytes = static_cast<uint32_t>((box1 ? 2 : 1) * P.a_box_rows * 128);
+        // the even CTA's barrier counts the bytes of both CTAs of a pair
+        const uint32_t bytes = CG == 2 ? a_block_bytes(P, 2 * tl.m) + a_block_bytes(P, 2 * tl.m + 1)
+                                       : a_block_bytes(P, mc);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty_a[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
@@ -166,17 +214,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             break;
           }
           uint8_t* sA = ring_a + (size_t)stage * kABytes;
-          mbar_arrive_expect_tx(&full_a[stage], bytes);
-          ++armed[stage];
-          tma_load_2d(sA, &P.tmA, &full_a[stage], kb * 64, arow, pol);
-          if (box1) tma_load_2d(sA + 64 * 128, &P.tmA, &full_a[stage], kb * 64, arow + P.a_box1_off, pol);
+          if (leader) {
+            mbar_arrive_expect_tx(&full_a[stage], bytes);
+            ++armed[stage];
+          }
+          if constexpr (CG == 2) {
+            const uint32_t fb = mapa_shared(smem_u32(&full_a[stage]), 0);
+            tma_load_2d_pair(sA, &P.tmA, fb, kb * 64, arow, pol);
+            if (box1) tma_load_2d_pair(sA + 64 * 128, &P.tmA, fb, kb * 64, arow + P.a_box1_off, pol);
+          } else {
+            tma_load_2d(sA, &P.tmA, &full_a[stage], kb * 64, arow, pol);
+            if (box1) tma_load_2d(sA + 64 * 128, &P.tmA, &full_a[stage], kb * 64, arow + P.a_box1_off, pol);
+          }
           if (++stage == SA) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) drain_ring(full_a, armed, SA, p.err);
+      if (!ok && leader) drain_ring(full_a, armed, SA, p.err);
     }
     __syncwarp();
   } else if (warp == 6) {
@@ -188,10 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
       int armed[kMaxStagesB];
       for (int s = 0; s < kMaxStagesB; ++s) armed[s] = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit0; t < total && ok; t += nunits) {
         Tile tl;
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
+        // a pair splits the N token rows: the even CTA holds the first half, the odd one the
+        // second (N is a multiple of 16, so each half is a multiple of 8 rows)
+        const int rows = CG == 2 ? tl.ncols >> 1 : tl.ncols;
+        const int r0 = tl.row0 + rank * rows;
         const uint32_t bytes = static_cast<uint32_t>(tl.ncols * 128);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -200,50 +260,55 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             break;
           }
           uint8_t* sB = ring_b + (size_t)stage * p.b_stage_bytes;
-          mbar_arrive_expect_tx(&full_b[stage], bytes);
-          ++armed[stage];
+          if (leader) {
+            mbar_arrive_expect_tx(&full_b[stage], bytes);
+            ++armed[stage];
+          }
+          const uint32_t fb = CG == 2 ? mapa_shared(smem_u32(&full_b[stage]), 0) : 0u;
           const int kx = kb * 64;
-          int off = 0, rem = tl.ncols;
-          while (rem >= 128) {
-            tma_load_2d(sB + off * 128, &P.tmB[0], &full_b[stage], kx, tl.row0 + off, pol_x);
-            off += 128;
-            rem -= 128;
+          int off = 0;
+          // boxes of 128, 64, 32, 16 and 8 rows cover any multiple of 8
+#pragma unroll 1
+          for (int b = 0, box = 128; b < 5; ++b, box >>= 1) {
+            const int nbox = b == 0 ? (rows - off) >> 7 : ((rows - off) >= box ? 1 : 0);
+            for (int i = 0; i < nbox; ++i) {
+              if constexpr (CG == 2)
+                tma_load_2d_pair(sB + off * 128, &P.tmB[b], fb, kx, r0 + off, pol_x);
+              else
+                tma_load_2d(sB + off * 128, &P.tmB[b], &full_b[stage], kx, r0 + off, pol_x);
+              off += box;
+            }
           }
-          if (rem & 64) {
-            tma_load_2d(sB + off * 128, &P.tmB[1], &full_b[stage], kx, tl.row0 + off, pol_x);
-            off += 64;
-          }
-          if (rem & 32) {
-            tma_load_2d(sB + off * 128, &P.tmB[2], &full_b[stage], kx, tl.row0 + off, pol_x);
-            off += 32;
-          }
-          if (rem & 16) tma_load_2d(sB + off * 128, &P.tmB[3], &full_b[stage], kx, tl.row0 + off, pol_x);
           if (++stage == SB) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) drain_ring(full_b, armed, SB, p.err);
+      if (!ok && leader) drain_ring(full_b, armed, SB, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
       int acc_i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit0; t < total && ok; t += nunits) {
         Tile tl;
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
-        const int buf = acc_i & 1;
-        const uint32_t use = static_cast<uint32_t>(acc_i >> 1);
-        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait)) break;
+        const int buf = acc_i % acc_bufs<CG>();
+        const uint32_t use = static_cast<uint32_t>(acc_i / acc_bufs<CG>());
+        // a pair's accumulator is free once the epilogues of both CTAs have read it
+        const bool freed =
+            CG == 2 ? mbar_wait_cluster(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait)
+                    : mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait);
+        if (!freed) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccCols);
-        const uint32_t idesc = idesc_bf16_f32(128, tl.ncols);
+        const uint32_t idesc = idesc_bf16_f32(128 * CG, tl.ncols);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full_a[sa], pa, abort_flag, p.err, kErrMmaWait) ||
@@ -256,9 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           const uint64_t bd = sdesc_k_sw128(smem_u32(ring_b + (size_t)sb * p.b_stage_bytes));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            mma_bf16(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
-          mma_commit(&empty_a[sa]);
-          mma_commit(&empty_b[sb]);
+            mma_bf16<CG>(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
+          mma_commit<CG>(&empty_a[sa]);
+          mma_commit<CG>(&empty_b[sb]);
           if (++sa == SA) {
             sa = 0;
             pa ^= 1u;
@@ -269,24 +334,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[buf]);
+        mma_commit<CG>(&tfull[buf]);
         ++acc_i;
       }
       // every MMA this thread issued completes before tensor memory is released
-      mma_commit(drain);
+      mma_commit<CG>(drain, 1);
       if (!drain_wait(drain, 0)) atomicCAS(p.err, 0, kErrDrainWait);
     }
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    const uint32_t tempty_lead[2] = {
+        CG == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
+        CG == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
     int acc_i = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = unit0; t < total; t += nunits) {
       Tile tl;
       decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
       const TcProblem& P = p.prob[tl.prob];
-      const int buf = acc_i & 1;
-      const uint32_t use = static_cast<uint32_t>(acc_i >> 1);
+      if (CG == 2) tl.m = 2 * tl.m + rank;  // this CTA's 128-row weight tile
+      const int buf = acc_i % acc_bufs<CG>();
+      const uint32_t use = static_cast<uint32_t>(acc_i / acc_bufs<CG>());
       const bool ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, p.err, kErrEpilogueWait);
       __syncwarp();
       if (named_bar_or(1, 128, !ok || *abort_flag != 0)) break;
@@ -295,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kAccCols);
       const int nchunks = (tl.valid + 31) >> 5;
       const int ep = threadIdx.x - 64;  // 0..127 across the four epilogue warps
-      if (MODE == kModeGateUp) {
+      if (tl.m >= P.m_cta) {
+        // the second tile of a pair past the end of the weight rows: nothing to store
+      } else if (MODE == kModeGateUp) {
         // Rows 0..63 of the accumulator are gate features, 64..127 the matching up features.
         // Per 16 tokens: every warp stages its 32 features x 16 tokens (fp32) token-major in
         // shared memory, then each thread computes 8 consecutive h features of one token and
@@ -378,17 +449,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
           }
         }
       }
+      // this warp's reads of the accumulator are done: one arrival per warp on the (even
+      // CTA's) accumulator-empty barrier
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2) mbar_arrive_remote(tempty_lead[buf]);
+        else mbar_arrive(&tempty[buf]);
+      }
       ++acc_i;
     }
   }
 
   __syncthreads();
+  // no CTA of a pair leaves (or frees tensor memory) while the pair's MMAs, TMA completions or
+  // remote arrivals may still touch it
+  if constexpr (CG == 2) cluster_sync();
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<CG>(tmem_base, tmem_cols<CG>());
   }
 }
 
@@ -411,38 +491,86 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MODE>
-cudaError_t launch_mode(const TcParams& p, int grid, size_t smem, cudaStream_t s) {
+// Opt-in shared memory of a kernel instance, set once per device.
+template <int MODE, int CG>
+cudaError_t configure(int dev) {
   static std::mutex mu;
-  static unsigned configured = 0;  // bit per device
+  static unsigned long long configured = 0;  // bit per device
+  std::lock_guard<std::mutex> g(mu);
+  if (dev < 64 && ((configured >> dev) & 1ull)) return cudaSuccess;
+  cudaError_t err = cudaFuncSetAttribute(
+      gemm_tc_kernel<MODE, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit(CG)));
+  // the whole unified L1/shared array as shared memory: two pair CTAs per SM need it
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(gemm_tc_kernel<MODE, CG>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+  if (err == cudaSuccess && dev < 64) configured |= 1ull << dev;
+  return err;
+}
+
+template <int MODE>
+cudaError_t launch_single(const TcParams& p, int sms, size_t smem, cudaStream_t s) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    if (dev < 32 && !((configured >> dev) & 1u)) {
-      err = cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemLimit));
-      if (err != cudaSuccess) return err;
-      configured |= 1u << dev;
-    } else if (dev >= 32) {
-      err = cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemLimit));
-      if (err != cudaSuccess) return err;
-    }
-  }
-  gemm_tc_kernel<MODE><<<grid, kThreads, smem, s>>>(p);
+  if ((err = configure<MODE, 1>(dev)) != cudaSuccess) return err;
+  gemm_tc_kernel<MODE, 1><<<sms, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaLaunchConfig_t pair_config(int grid, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// CTA pairs resident at once: the persistent grid.  A pair CTA's shared-memory budget (at most
+// kSmemLimitPair) leaves room for two of them per SM, so two pairs run on each TPC.  The
+// occupancy queries of the runtime report one cluster per TPC for this kernel, yet a grid of
+// two pairs per TPC measures almost twice the MMA rate of one, so the count is taken from the
+// budget.  Were it ever too high the extra pairs would only wait for a free TPC (the tiles are
+// statically strided over pairs and no pair waits for another), costing time, not results.
+int resident_pairs(int sms, size_t smem) {
+  const int per_sm = smem <= kSmemLimitPair ? ctas_per_sm<2>() : 1;
+  return per_sm * (sms / 2);
+}
+
+template <int MODE>
+cudaError_t launch_pair(const TcParams& p, int sms, size_t smem, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if ((err = configure<MODE, 2>(dev)) != cudaSuccess) return err;
+  const int pairs = resident_pairs(sms, smem);
+  if (pairs < 1) return cudaErrorInvalidConfiguration;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2 * pairs, smem, s, attr);
+  err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, 2>, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // Ring depths for an n-tile cap: the token ring holds a few stages (its loads hit L2), the
-// weight ring takes the rest of shared memory (its loads come from HBM).
+// weight ring takes the rest of shared memory (its loads come from HBM).  A CTA of a pair
+// holds half of each token tile and shares its SM with a second pair CTA, so it has half the
+// shared memory.
 void gemm_tc_plan(int bn, int n_seg, TcParams& p) {
-  p.b_stage_bytes = bn * 128;
-  p.stages_b = bn >= 128 ? 3 : 4;
-  const size_t avail = kSmemLimit - fixed_smem_bytes(n_seg) - (size_t)p.stages_b * p.b_stage_bytes;
+  const int rows = p.cg == 2 ? bn / 2 : bn;
+  p.b_stage_bytes = rows * 128;
+  if (p.cg == 2) p.stages_b = bn >= 128 ? 3 : kMaxStagesB;
+  else p.stages_b = bn >= 128 ? 3 : 4;
+  const size_t avail = smem_limit(p.cg) - fixed_smem_bytes(n_seg) - (size_t)p.stages_b * p.b_stage_bytes;
   int sa = static_cast<int>(avail / kABytes);
   p.stages_a = sa > kMaxStagesA ? kMaxStagesA : sa;
 }
@@ -451,7 +579,7 @@ size_t gemm_tc_smem_bytes(const TcParams& p) {
   const int n_seg = p.prob[0].seg_off != nullptr ? p.prob[0].n_seg : 0;
   size_t b = fixed_smem_bytes(n_seg) + (size_t)p.stages_a * kABytes +
              (size_t)p.stages_b * p.b_stage_bytes;
-  return b < kSmemFloor ? kSmemFloor : b;
+  return p.cg == 1 && b < kSmemFloor ? kSmemFloor : b;
 }
 
 int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
@@ -468,15 +596,19 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
-cudaError_t launch_gemm_tc(int mode, const TcParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s) {
   const size_t smem = gemm_tc_smem_bytes(p);
-  if (smem > kSmemLimit || p.stages_a < 2 || p.stages_b < 2 || p.stages_a > kMaxStagesA ||
-      p.stages_b > kMaxStagesB)
+  if (smem > smem_limit(p.cg) || p.stages_a < 2 || p.stages_b < 2 || p.stages_a > kMaxStagesA ||
+      p.stages_b > kMaxStagesB || (p.cg != 1 && p.cg != 2) || (p.cg == 2 && mode == kModeRouter))
     return cudaErrorInvalidConfiguration;
+  if (p.cg == 2) {
+    if (mode == kModeGateUp) return launch_pair<kModeGateUp>(p, sms, smem, s);
+    return launch_pair<kModeDown>(p, sms, smem, s);
+  }
   switch (mode) {
-    case kModeRouter: return launch_mode<kModeRouter>(p, grid, smem, s);
-    case kModeGateUp: return launch_mode<kModeGateUp>(p, grid, smem, s);
-    default: return launch_mode<kModeDown>(p, grid, smem, s);
+    case kModeRouter: return launch_single<kModeRouter>(p, sms, smem, s);
+    case kModeGateUp: return launch_single<kModeGateUp>(p, sms, smem, s);
+    default: return launch_single<kModeDown>(p, sms, smem, s);
   }
 }
 

@@ -14,6 +14,7 @@ enum DeviceErr {
   kErrMmaWait = 2,
   kErrEpilogueWait = 3,
   kErrDrainWait = 4,
+  kErrLaunchShape = 5,  // a CTA-pair kernel was launched without 2-CTA clusters
 };
 
 // Epilogues of the tensor-core grouped GEMM.
@@ -29,12 +30,13 @@ constexpr int kDispatchWarps = 8;
 // swizzle; the product is D = A * B^T accumulated in fp32 in tensor memory.
 struct TcProblem {
   CUtensorMap tmA;     // weights [rows][K]: box 64 columns x a_box_rows rows
-  CUtensorMap tmB[4];  // tokens  [rows][K]: boxes of 128 / 64 / 32 / 16 rows x 64 columns
+  CUtensorMap tmB[5];  // tokens  [rows][K]: boxes of 128 / 64 / 32 / 16 / 8 rows x 64 columns
   void* out;
   const int* seg_off;  // grouped: device [n_seg+1] first B row of each segment; null = single
   const int* ntp;      // grouped: device [n_seg+1] prefix of n-tiles per segment
   int K;               // reduction length, multiple of 64
-  int m_tiles;         // 128-row weight tiles per segment
+  int m_tiles;         // scheduled m-tiles per segment: weight tiles of one CTA, or of a pair
+  int m_cta;           // 128-row weight tiles per segment (a pair's second tile may be past it)
   int group;           // m-tiles scheduled together (divides m_tiles)
   int a_seg_stride;    // A rows between segments
   int a_m_stride;      // A rows between m-tiles
@@ -52,17 +54,19 @@ struct TcProblem {
 struct TcParams {
   TcProblem prob[2];
   int n_prob;
+  int cg;             // CTAs per MMA: 1, or 2 (a CTA pair, tcgen05 cta_group::2, M = 256)
   int bn;             // n-tile cap: multiple of 16, at most 256
   int stages_a;       // depth of the weight ring (16 KiB stages)
   int stages_b;       // depth of the token ring
-  int b_stage_bytes;  // bn * 128 B
+  int b_stage_bytes;  // B rows one CTA holds per stage (bn, or bn / 2 for a pair) * 128 B
   int* err;           // device status word
 };
 
 // Tensor-core GEMM (moe_gemm_tc.cu).
 size_t gemm_tc_smem_bytes(const TcParams& p);
 void gemm_tc_plan(int bn, int n_seg, TcParams& p);
-cudaError_t launch_gemm_tc(int mode, const TcParams& p, int grid, cudaStream_t s);
+// Launches one GEMM: `sms` CTAs (cg 1), or as many 2-CTA clusters as fit at once (cg 2).
+cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s);
 int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);
 

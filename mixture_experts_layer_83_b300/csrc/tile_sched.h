@@ -15,7 +15,7 @@ namespace moe {
 struct Tile {
   int prob;   // 0 = first operand set (grouped or single), 1 = second (single)
   int seg;    // segment (expert) within the operand set
-  int m;      // 128-row weight tile index within the segment
+  int m;      // scheduled m-tile within the segment (a pair's tiles are 2m and 2m + 1)
   int row0;   // first B row of the tile
   int ncols;  // MMA N: multiple of 16, at most the n-tile cap
   int valid;  // B rows of the tile that belong to the segment (<= ncols)
@@ -74,9 +74,14 @@ MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, i
   tl.valid = left < tl.ncols ? left : tl.ncols;
 }
 
-// Whether a tile loads the second 64-row weight box.
-MOE_HD bool tile_has_box1(const TcProblem& P, const Tile& tl) {
-  return P.a_box_rows == 64 && (tl.m * P.a_m_stride + P.a_box1_off) < P.a_valid_rows;
+// Whether the CTA that owns 128-row weight tile `m` loads the second 64-row weight box.
+MOE_HD bool a_has_box1(const TcProblem& P, int m) {
+  return P.a_box_rows == 64 && (m * P.a_m_stride + P.a_box1_off) < P.a_valid_rows;
+}
+
+// Weight bytes the CTA that owns weight tile `m` loads per 64-deep k-block.
+MOE_HD unsigned a_block_bytes(const TcProblem& P, int m) {
+  return static_cast<unsigned>((a_has_box1(P, m) ? 2 : 1) * P.a_box_rows * 128);
 }
 
 }  // namespace moe

@@ -112,8 +112,10 @@ def test_status_strings_and_launch_count():
 # ------------------------------------------------------------------ tile schedule
 def _check_schedule(s, which, counts):
     tiles, geo = moe.moe_debug_gemm_tiles(s, which, counts)
-    assert 2 <= geo["stages_a"] <= 12 and 2 <= geo["stages_b"] <= 4
-    assert geo["smem_bytes"] <= 232448
+    assert 2 <= geo["stages_a"] <= 12 and 2 <= geo["stages_b"] <= 8
+    assert geo["cg"] == (1 if which == 0 else 2)
+    # one-CTA GEMMs may use the 227 KiB opt-in; pair CTAs share their SM with a second one
+    assert geo["smem_bytes"] <= (232448 if geo["cg"] == 1 else 114688)
     bn = geo["bn"]
     assert bn % 16 == 0 and 16 <= bn <= 256
     if which == 0:
@@ -149,6 +151,19 @@ def _check_schedule(s, which, counts):
     if which > 0 and s.Fs > 0:
         want += m_tiles[1] * s.T
     assert len(covered) == want
+    if geo["cg"] == 2:
+        # the CTAs of a pair share the token rows: tile 2j is listed with its partner 2j + 1
+        # right after it, unless 2j + 1 is past the weight rows
+        t = tiles.tolist()
+        i = 0
+        while i < len(t):
+            prob, seg, m, row0, ncols = t[i][:5]
+            assert m % 2 == 0
+            if m + 1 < m_tiles[prob]:
+                assert t[i + 1][:5] == [prob, seg, m + 1, row0, ncols]
+                i += 2
+            else:
+                i += 1
 
 
 @pytest.mark.parametrize("which", [1, 2])
@@ -184,8 +199,8 @@ def test_router_gemm_schedule_covers_every_row_once(T, E):
 def test_prefill_geometry_uses_full_width_tiles():
     s = shape(T=8192, d=7168, E=256, k=8, F=2048, Fs=2048)
     _, geo = moe.moe_debug_gemm_tiles(s, 1, np.full(256, 256))
-    assert geo["bn"] == 256 and geo["stages_a"] == 7 and geo["stages_b"] == 3
-    assert geo["m_tiles0"] == 32
+    assert geo["bn"] == 256 and geo["stages_a"] == 3 and geo["stages_b"] == 3
+    assert geo["m_tiles0"] == 32 and geo["cg"] == 2
     _, geo = moe.moe_debug_gemm_tiles(shape(T=128, d=7168, E=256, k=8, F=2048, Fs=2048), 1,
                                       np.full(256, 4))
-    assert geo["bn"] == 32 and geo["stages_a"] == 12 and geo["stages_b"] == 4
+    assert geo["bn"] == 32 and geo["stages_a"] == 5 and geo["stages_b"] == 8
