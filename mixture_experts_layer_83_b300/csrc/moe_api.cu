@@ -28,7 +28,7 @@ constexpr int kMaxK = 32;
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  size_t status, logits, topk_idx, topk_w, chunk, offsets, ntp, sorted, slot, xs_y, h, h_sh, total;
+  size_t status, logits, topk_idx, topk_w, chunk, offsets, ntp, ntp2, sorted, slot, xs_y, h, h_sh, total;
 };
 
 // Workspace carve-up.  xs (gathered rows) and y (expert outputs, routed rows then the shared
@@ -52,6 +52,7 @@ Layout layout_of(const moe_shape& s) {
   w.chunk = take(nch * s.E * 4);
   w.offsets = take((size_t)(s.E + 1) * 4);
   w.ntp = take((size_t)(s.E + 1) * 4);
+  w.ntp2 = take((size_t)(s.E + 1) * 4);
   w.sorted = take(R * 4);
   w.slot = take(R * 4);
   w.xs_y = take((R + tsh) * s.d * elt);
@@ -106,13 +107,22 @@ int largest_group(int m_tiles) {
   return 1;
 }
 
-// n-tile cap of the expert GEMMs: twice the mean rows per expert, 32..256.
+// n-tile cap of the down GEMM: twice the mean rows per expert, 32..256.
 int expert_bn(const moe_shape& s) {
   const long long R = (long long)s.T * s.k;
   const int avg = (int)((R + s.E - 1) / s.E);
   int bn = pow2_at_least(avg * 2 > 32 ? avg * 2 : 32);
   return bn > 256 ? 256 : bn;
 }
+
+// Whether the gate/up GEMM runs on wide pairs: when experts average more than 64 rows (a
+// prefill batch), a segment of up to twice the mean rows then shares one pass over the
+// expert's weights.  Smaller segments (decode) stream weights with more producers per SM on
+// two narrow pairs per TPC instead.
+bool gateup_wide(const moe_shape& s) { return expert_bn(s) >= 256; }
+
+// n-tile cap of the gate/up GEMM: twice the down GEMM's (512) on wide pairs, the same otherwise.
+int gateup_bn(const moe_shape& s) { return gateup_wide(s) ? 2 * expert_bn(s) : expert_bn(s); }
 
 // n-tile cap of the router GEMM: about one tile per SM.
 int router_bn(const moe_shape& s, int sms) {
@@ -166,9 +176,10 @@ void set_m_tiles(TcProblem& P, int m_cta, int cg) {
 
 void geometry_gateup(const moe_shape& s, TcParams& p) {
   memset(&p, 0, sizeof(p));
-  const int bn = expert_bn(s);
+  const int bn = gateup_bn(s);
   p.n_prob = s.Fs > 0 ? 2 : 1;
   p.cg = 2;
+  p.wide = gateup_wide(s) ? 1 : 0;
   p.bn = bn;
   TcProblem& P = p.prob[0];
   P.a_box_rows = 64;
@@ -242,6 +253,7 @@ int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const voi
   int* status = reinterpret_cast<int*>(ws + L.status);
   int* offsets = reinterpret_cast<int*>(ws + L.offsets);
   int* ntp = reinterpret_cast<int*>(ws + L.ntp);
+  int* ntp2 = reinterpret_cast<int*>(ws + L.ntp2);
   void* xs_y = ws + L.xs_y;
   void* h = ws + L.h;
   void* h_sh = ws + L.h_sh;
@@ -260,7 +272,7 @@ int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const voi
   pg.err = status;
   pg.prob[0].out = h;
   pg.prob[0].seg_off = offsets;
-  pg.prob[0].ntp = ntp;
+  pg.prob[0].ntp = ntp2;  // gate/up tiles the segments with its own n-tile cap
   if (encode_tmap_bf16(&pg.prob[0].tmA, w_gate_up, (uint64_t)E * 2 * F, (uint64_t)d, 64) != 0 ||
       encode_tokens(pg.prob[0], xs_y, R, d) != 0)
     return -1;
@@ -335,6 +347,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   int* chunk = reinterpret_cast<int*>(ws + L.chunk);
   int* offsets = reinterpret_cast<int*>(ws + L.offsets);
   int* ntp = reinterpret_cast<int*>(ws + L.ntp);
+  int* ntp2 = reinterpret_cast<int*>(ws + L.ntp2);
   int* sorted = sorted_token_out ? sorted_token_out : reinterpret_cast<int*>(ws + L.sorted);
   int* slot = reinterpret_cast<int*>(ws + L.slot);
   void* xs_y = ws + L.xs_y;
@@ -363,8 +376,8 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   MOE_TRY(launch_topk(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, logits, nullptr, bias, S.T, S.E, S.k,
                       tidx, tw, stream));
   if (!mark(2)) return MOE_ERR_CUDA;
-  MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp, sorted, slot,
-                          stream));
+  MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp,
+                          bf16 ? gateup_bn(S) : 0, bf16 ? ntp2 : nullptr, sorted, slot, stream));
   if (!mark(3)) return MOE_ERR_CUDA;
   MOE_TRY(launch_gather(x, sorted, R, S.d, bf16 ? 2 : 4, xs_y, stream));
   if (!mark(4)) return MOE_ERR_CUDA;
@@ -454,8 +467,8 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
-                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp),
-                      sorted_token, slot_pos, stream) != cudaSuccess)
+                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0,
+                      nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

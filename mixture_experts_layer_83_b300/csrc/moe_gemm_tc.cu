@@ -19,7 +19,8 @@
 //           even CTA's barriers; its MMA issuer runs the pair and its commits arrive on both
 //           CTAs' barriers (multicast).
 //
-// Roles (224 threads, one CTA per SM, persistent over a static tile stride):
+// Roles (persistent over a static tile stride; warps 0..6, plus warps 7..11 for a wide pair,
+// plus extra producer warps for the pair forms):
 //   warp 0 lane 0   weight producer: TMA of the 128 x 64 weight block of each k-step into
 //                   the weight ring (16 KiB stages, up to 12 deep): weights come from HBM
 //                   and need the longest look-ahead
@@ -53,29 +54,59 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 224;
 constexpr int kMaxStagesA = 12;
 constexpr int kMaxStagesB = 8;
 constexpr int kAccCols = 256;  // one accumulator: 128 lanes x up to 256 fp32 columns
-// One CTA per SM (CG = 1) double-buffers its accumulator in all 512 TMEM columns.  CTA pairs
-// (CG = 2) run two per SM (two pairs per TPC), each with one accumulator of 256 columns: the
-// second pair keeps the tensor cores busy while the first drains its accumulator, and the
-// two MMA issuers per SM halve the per-instruction issue cost that bounds MMAs with N < 256.
-template <int CG> constexpr int acc_bufs() { return CG == 2 ? 1 : 2; }
-template <int CG> constexpr uint32_t tmem_cols() { return static_cast<uint32_t>(acc_bufs<CG>() * kAccCols); }
-template <int CG> constexpr int ctas_per_sm() { return CG == 2 ? 2 : 1; }
+// Three forms share this kernel:
+//   one CTA (CG = 1, router): one CTA per SM, accumulator double-buffered in 512 TMEM columns.
+//   narrow pair (CG = 2, down): two pairs per TPC (two CTAs per SM), one 256-column
+//     accumulator each; the second pair keeps the tensor cores busy while the first drains its
+//     accumulator, and two MMA issuers per SM halve the per-instruction issue cost (about 125
+//     cycles per tcgen05.mma from one thread) that otherwise bounds MMAs with N < 256.
+//   wide pair (CG = 2, WIDE, gate/up): one pair per TPC, n-tiles of up to 512 token rows in one
+//     512-column accumulator, split over two MMA issuers (one per 256-column half) and two
+//     epilogue groups.  An expert's whole token segment (up to 512 rows) shares one pass over
+//     its weights, so each weight tile is streamed from HBM once.
+// Producer threads per ring.  One thread's TMA issue bounds the stream it keeps in flight, so
+// the pair forms spread each ring over several producer warps.  Producer pid owns the ring
+// stages s with s % producers == pid and fills their rounds in order: every stage keeps a
+// single producer, so a producer can never be two rounds ahead on a stage (where the parity
+// of an mbarrier wait would no longer tell the rounds apart).  Ring depths are multiples of
+// the producer counts.
+template <int CG, int WIDE> constexpr int producers_a() { return CG == 2 ? 2 : 1; }
+template <int CG, int WIDE> constexpr int producers_b() { return WIDE ? 4 : (CG == 2 ? 2 : 1); }
+// Warps 0..6 (0..11 for a wide pair) have fixed roles; the extra producers follow them.
+template <int WIDE> constexpr int base_warps() { return WIDE ? 12 : 7; }
+template <int CG, int WIDE> constexpr int threads_of() {
+  return 32 * (base_warps<WIDE>() + producers_a<CG, WIDE>() - 1 + producers_b<CG, WIDE>() - 1);
+}
+template <int CG, int WIDE> constexpr int acc_bufs() { return CG == 1 ? 2 : 1; }
+template <int CG, int WIDE> constexpr uint32_t tmem_cols() { return CG == 2 && !WIDE ? 256u : 512u; }
+template <int CG, int WIDE> constexpr int ctas_per_sm() { return CG == 2 && !WIDE ? 2 : 1; }
+
+// Token columns of the two MMAs of a wide tile: n0 = the first half rounded up to 16 rows
+// (all of a tile that fits one accumulator half), n1 = the rest.
+struct NSplit {
+  int n0, n1;
+};
+template <int WIDE>
+__device__ __forceinline__ NSplit n_split(int ncols) {
+  if (!WIDE || ncols <= kAccCols) return NSplit{ncols, 0};
+  const int n0 = (((ncols >> 4) + 1) >> 1) << 4;
+  return NSplit{n0, ncols - n0};
+}
 constexpr int kABytes = 128 * 128;       // weight stage: 128 rows x 64 bf16
 constexpr int kStageLdF = 68;            // fp32 row of the gate/up staging (64 + pad)
 constexpr int kStageLdH = 136;           // bf16 row of the down staging (128 + pad)
 constexpr int kXchgFloats = 2 * 16 * kStageLdF;  // 8704 B, also holds 32 x kStageLdH bf16
 static_assert(32 * kStageLdH * 2 <= kXchgFloats * 4, "down staging fits the epilogue buffer");
-constexpr int kBarBytes = 512;           // 2 * (12 + 8) + 5 mbarriers, rounded
-static_assert(8 * (2 * (kMaxStagesA + kMaxStagesB) + 5) <= kBarBytes, "mbarriers fit");
+constexpr int kBarBytes = 512;           // 2 * (12 + 8) + 6 mbarriers, rounded
+static_assert(8 * (2 * (kMaxStagesA + kMaxStagesB) + 6) <= kBarBytes, "mbarriers fit");
 constexpr int kMiscBytes = 128;
 constexpr size_t kSmemLimit = 232448;    // 227 KiB opt-in per CTA
 constexpr size_t kSmemLimitPair = 112 * 1024;  // two per SM with room to spare in its 228 KiB
 constexpr size_t kSmemFloor = 120 * 1024;  // keeps a second one-CTA kernel (and its TMEM demand) off the SM
-size_t smem_limit(int cg) { return cg == 2 ? kSmemLimitPair : kSmemLimit; }
+size_t smem_limit(int cg, int wide) { return cg == 2 && !wide ? kSmemLimitPair : kSmemLimit; }
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -102,8 +133,9 @@ __device__ void drain_ring(uint64_t* full, const int* armed, int stages, int* er
   }
 }
 
-template <int MODE, int CG>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+template <int MODE, int CG, int WIDE>
+__global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>())
+    gemm_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   if constexpr (CG == 2) {
     // a pair kernel launched without 2-CTA clusters: record it and leave before any shared
@@ -113,6 +145,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
       return;
     }
   }
+  constexpr int kGroups = WIDE ? 2 : 1;           // epilogue groups of four warps
+  constexpr int kIssuers = WIDE ? 2 : 1;          // MMA issuing threads
+  constexpr int kBufs = acc_bufs<CG, WIDE>();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int SA = p.stages_a, SB = p.stages_b;
@@ -125,11 +160,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
   uint64_t* empty_b = full_b + kMaxStagesB;
   uint64_t* tfull = empty_b + kMaxStagesB;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* drain = tempty + 2;  // one per issuer
   int* misc = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
   volatile int* abort_flag = misc + 1;
-  float* xchg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(misc) + kMiscBytes);
-  int* s_seg = reinterpret_cast<int*>(xchg + kXchgFloats);
+  float* xchg0 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(misc) + kMiscBytes);
+  int* s_seg = reinterpret_cast<int*>(xchg0 + kGroups * kXchgFloats);
   const int n_seg0 = p.prob[0].seg_off != nullptr ? p.prob[0].n_seg : 0;
   int* s_ntp = s_seg + (n_seg0 + 1);
 
@@ -141,19 +176,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
   const int nunits = CG == 2 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
+    // every ring stage and accumulator is released by each MMA issuer once
     for (int s = 0; s < SA; ++s) {
       mbar_init(&full_a[s], 1);
-      mbar_init(&empty_a[s], 1);
+      mbar_init(&empty_a[s], kIssuers);
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(&full_b[s], 1);
-      mbar_init(&empty_b[s], 1);
+      mbar_init(&empty_b[s], kIssuers);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4 * CG);  // one arrival per epilogue warp of each CTA
+      mbar_init(&tfull[b], kIssuers);
+      mbar_init(&tempty[b], 4 * kGroups * CG);  // one arrival per epilogue warp of each CTA
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -164,11 +201,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
     }
   }
   if (warp == 0) {
-    tmem_alloc<CG>(reinterpret_cast<uint32_t*>(misc), tmem_cols<CG>());
+    tmem_alloc<CG>(reinterpret_cast<uint32_t*>(misc), tmem_cols<CG, WIDE>());
     tmem_relinquish<CG>();
   }
   if (n_seg0 > 0) {
-    for (int i = threadIdx.x; i <= n_seg0; i += kThreads) {
+    for (int i = threadIdx.x; i <= n_seg0; i += threads_of<CG, WIDE>()) {
       s_seg[i] = p.prob[0].seg_off[i];
       s_ntp[i] = p.prob[0].ntp[i];
     }
@@ -184,8 +221,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
   const int tiles1 = p.n_prob > 1 ? p.prob[1].nt * p.prob[1].m_tiles : 0;
   const int total = tiles0 + tiles1;
 
+  constexpr int kProdA = producers_a<CG, WIDE>(), kProdB = producers_b<CG, WIDE>();
+  // producer ids: weight ring (warp 0, then the first extra warps), token ring (warp 6, then the
+  // rest)
+  int a_pid = -1, b_pid = -1;
   if (warp == 0) {
-    // ---------------------------------------------------------------- weight producer
+    a_pid = 0;
+  } else if (warp == 6) {
+    b_pid = 0;
+  } else if (warp >= base_warps<WIDE>()) {
+    const int x = warp - base_warps<WIDE>();
+    if (x < kProdA - 1) a_pid = x + 1;
+    else b_pid = x - (kProdA - 1) + 1;
+  }
+  if (a_pid >= 0) {
+    // ---------------------------------------------------------------- weight producer(s)
+    const int pid = a_pid;
     if (lane == 0) {
       // weights read by one tile only stream through L2 (evict first); weights a neighbouring
       // n-tile reads again stay at normal priority
@@ -209,6 +260,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
                                        : a_block_bytes(P, mc);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (stage % kProdA != pid) {  // another producer's stage
+            if (++stage == SA) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait(&empty_a[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
             ok = false;
             break;
@@ -235,8 +293,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
       if (!ok && leader) drain_ring(full_a, armed, SA, p.err);
     }
     __syncwarp();
-  } else if (warp == 6) {
-    // ---------------------------------------------------------------- token producer
+  } else if (b_pid >= 0) {
+    // ---------------------------------------------------------------- token producer(s)
+    const int pid = b_pid;
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();  // re-read by every weight tile
       int stage = 0;
@@ -248,13 +307,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
         Tile tl;
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
-        // a pair splits the N token rows: the even CTA holds the first half, the odd one the
-        // second (N is a multiple of 16, so each half is a multiple of 8 rows)
-        const int rows = CG == 2 ? tl.ncols >> 1 : tl.ncols;
-        const int r0 = tl.row0 + rank * rows;
+        const NSplit ns = n_split<WIDE>(tl.ncols);
         const uint32_t bytes = static_cast<uint32_t>(tl.ncols * 128);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (stage % kProdB != pid) {  // another producer's stage
+            if (++stage == SB) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!mbar_wait(&empty_b[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
             ok = false;
             break;
@@ -266,18 +329,29 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
           }
           const uint32_t fb = CG == 2 ? mapa_shared(smem_u32(&full_b[stage]), 0) : 0u;
           const int kx = kb * 64;
-          int off = 0;
-          // boxes of 128, 64, 32, 16 and 8 rows cover any multiple of 8
+          // each MMA's N token rows are split over a pair: the even CTA holds the first half,
+          // the odd one the second (N is a multiple of 16, so each half is a multiple of 8);
+          // a wide tile's second MMA follows the first in the stage
+          int soff = 0;  // shared-memory row of this CTA's stage
 #pragma unroll 1
-          for (int b = 0, box = 128; b < 5; ++b, box >>= 1) {
-            const int nbox = b == 0 ? (rows - off) >> 7 : ((rows - off) >= box ? 1 : 0);
-            for (int i = 0; i < nbox; ++i) {
-              if constexpr (CG == 2)
-                tma_load_2d_pair(sB + off * 128, &P.tmB[b], fb, kx, r0 + off, pol_x);
-              else
-                tma_load_2d(sB + off * 128, &P.tmB[b], &full_b[stage], kx, r0 + off, pol_x);
-              off += box;
+          for (int h = 0; h < kIssuers; ++h) {
+            const int nh = h == 0 ? ns.n0 : ns.n1;
+            const int rows = CG == 2 ? nh >> 1 : nh;
+            const int g0 = tl.row0 + (h == 0 ? 0 : ns.n0) + rank * rows;
+            int off = 0;
+            // boxes of 128, 64, 32, 16 and 8 rows cover any multiple of 8
+#pragma unroll 1
+            for (int b = 0, box = 128; b < 5; ++b, box >>= 1) {
+              const int nbox = b == 0 ? (rows - off) >> 7 : ((rows - off) >= box ? 1 : 0);
+              for (int i = 0; i < nbox; ++i) {
+                if constexpr (CG == 2)
+                  tma_load_2d_pair(sB + (soff + off) * 128, &P.tmB[b], fb, kx, g0 + off, pol_x);
+                else
+                  tma_load_2d(sB + (soff + off) * 128, &P.tmB[b], &full_b[stage], kx, g0 + off, pol_x);
+                off += box;
+              }
             }
+            soff += rows;
           }
           if (++stage == SB) {
             stage = 0;
@@ -288,8 +362,11 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
       if (!ok && leader) drain_ring(full_b, armed, SB, p.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || (WIDE && warp == 7)) {
+    // ---------------------------------------------------------------- MMA issuer(s)
+    // Issuer h owns MMAs over token columns [h ? n0 : 0, +n_h) into accumulator columns
+    // [h * 256, +n_h); both wait for every stage and release it after their MMAs.
+    const int h = warp == 1 ? 0 : 1;
     if (lane == 0 && leader) {
       int sa = 0, sb = 0;
       uint32_t pa = 0, pb = 0;
@@ -299,16 +376,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
         Tile tl;
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
-        const int buf = acc_i % acc_bufs<CG>();
-        const uint32_t use = static_cast<uint32_t>(acc_i / acc_bufs<CG>());
+        const NSplit ns = n_split<WIDE>(tl.ncols);
+        const int nh = h == 0 ? ns.n0 : ns.n1;
+        const int brow = h == 0 ? 0 : (CG == 2 ? ns.n0 >> 1 : ns.n0);  // stage row of this MMA's B
+        const int buf = acc_i % kBufs;
+        const uint32_t use = static_cast<uint32_t>(acc_i / kBufs);
         // a pair's accumulator is free once the epilogues of both CTAs have read it
         const bool freed =
             CG == 2 ? mbar_wait_cluster(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait)
                     : mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p.err, kErrMmaWait);
         if (!freed) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccCols);
-        const uint32_t idesc = idesc_bf16_f32(128 * CG, tl.ncols);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * kAccCols + h * kAccCols);
+        const uint32_t idesc = idesc_bf16_f32(128 * CG, nh > 0 ? nh : 16);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full_a[sa], pa, abort_flag, p.err, kErrMmaWait) ||
@@ -317,11 +397,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)sa * kABytes));
-          const uint64_t bd = sdesc_k_sw128(smem_u32(ring_b + (size_t)sb * p.b_stage_bytes));
+          if (nh > 0) {
+            const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)sa * kABytes));
+            const uint64_t bd =
+                sdesc_k_sw128(smem_u32(ring_b + (size_t)sb * p.b_stage_bytes + (size_t)brow * 128));
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_bf16<CG>(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
+            for (int j = 0; j < 4; ++j)
+              mma_bf16<CG>(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
+          }
           mma_commit<CG>(&empty_a[sa]);
           mma_commit<CG>(&empty_b[sb]);
           if (++sa == SA) {
@@ -338,13 +421,19 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
         ++acc_i;
       }
       // every MMA this thread issued completes before tensor memory is released
-      mma_commit<CG>(drain, 1);
-      if (!drain_wait(drain, 0)) atomicCAS(p.err, 0, kErrDrainWait);
+      mma_commit<CG>(&drain[h], 1);
+      if (!drain_wait(&drain[h], 0)) atomicCAS(p.err, 0, kErrDrainWait);
     }
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    // Group g (warps 2..5, and 8..11 of a wide tile) reads accumulator half g; each warp may
+    // only access its tensor-memory lane quarter (warp % 4).
+    const int g = warp >= 8 ? 1 : 0;
+    const int q = warp & 3;
+    const int ep = threadIdx.x - (g == 0 ? 64 : 256);  // 0..127 within the group
+    const int bar_or = 1 + 2 * g, bar_sync = 2 + 2 * g;
+    float* xchg = xchg0 + g * kXchgFloats;
     const uint32_t tempty_lead[2] = {
         CG == 2 ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
         CG == 2 ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
@@ -354,18 +443,24 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
       decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
       const TcProblem& P = p.prob[tl.prob];
       if (CG == 2) tl.m = 2 * tl.m + rank;  // this CTA's 128-row weight tile
-      const int buf = acc_i % acc_bufs<CG>();
-      const uint32_t use = static_cast<uint32_t>(acc_i / acc_bufs<CG>());
+      const NSplit ns = n_split<WIDE>(tl.ncols);
+      const int buf = acc_i % kBufs;
+      const uint32_t use = static_cast<uint32_t>(acc_i / kBufs);
       const bool ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, p.err, kErrEpilogueWait);
       __syncwarp();
-      if (named_bar_or(1, 128, !ok || *abort_flag != 0)) break;
+      if (named_bar_or(bar_or, 128, !ok || *abort_flag != 0)) break;
       tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * kAccCols);
-      const int nchunks = (tl.valid + 31) >> 5;
-      const int ep = threadIdx.x - 64;  // 0..127 across the four epilogue warps
-      if (tl.m >= P.m_cta) {
-        // the second tile of a pair past the end of the weight rows: nothing to store
+      // this group's token columns: [c0, c0 + valid) of the tile, at accumulator column acol
+      const int c0 = g == 0 ? 0 : ns.n0;
+      const int width = g == 0 ? ns.n0 : ns.n1;
+      int valid = tl.valid - c0;
+      valid = valid < 0 ? 0 : (valid > width ? width : valid);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(buf * kAccCols + g * kAccCols);
+      const int nchunks = (valid + 31) >> 5;
+      const int rowb = P.out_row_base + tl.row0 + c0;  // output row of this group's column 0
+      if (tl.m >= P.m_cta || valid == 0) {
+        // the second tile of a pair past the end of the weight rows, or no columns here
       } else if (MODE == kModeGateUp) {
         // Rows 0..63 of the accumulator are gate features, 64..127 the matching up features.
         // Per 16 tokens: every warp stages its 32 features x 16 tokens (fp32) token-major in
@@ -383,30 +478,29 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int col0 = c * 32 + half * 16;
-            if (col0 >= tl.valid) break;  // uniform over the 128 epilogue threads
+            if (col0 >= valid) break;  // uniform over the group's 128 threads
 #pragma unroll
             for (int j = 0; j < 16; ++j) mine[j * kStageLdF + fl] = __uint_as_float(v[half * 16 + j]);
-            named_bar_sync(2, 128);
+            named_bar_sync(bar_sync, 128);
             const int col = col0 + tt;
-            if (col < tl.valid) {
+            if (col < valid) {
               const float4* g4 = reinterpret_cast<const float4*>(gs + tt * kStageLdF + fg * 8);
               const float4* u4 = reinterpret_cast<const float4*>(us + tt * kStageLdF + fg * 8);
               const float4 ga = g4[0], gb = g4[1], ua = u4[0], ub = u4[1];
-              const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-              const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+              const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+              const float uv[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
               uint4 o;
               __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float h0 = __fdividef(g[2 * i] * u[2 * i], 1.f + __expf(-g[2 * i]));
+                const float h0 = __fdividef(gv[2 * i] * uv[2 * i], 1.f + __expf(-gv[2 * i]));
                 const float h1 =
-                    __fdividef(g[2 * i + 1] * u[2 * i + 1], 1.f + __expf(-g[2 * i + 1]));
+                    __fdividef(gv[2 * i + 1] * uv[2 * i + 1], 1.f + __expf(-gv[2 * i + 1]));
                 oh[i] = __floats2bfloat162_rn(h0, h1);
               }
-              *reinterpret_cast<uint4*>(hout + (size_t)(P.out_row_base + tl.row0 + col) * P.out_ld +
-                                        tl.m * 64 + fg * 8) = o;
+              *reinterpret_cast<uint4*>(hout + (size_t)(rowb + col) * P.out_ld + tl.m * 64 + fg * 8) = o;
             }
-            named_bar_sync(2, 128);
+            named_bar_sync(bar_sync, 128);
           }
         }
       } else if (MODE == kModeDown) {
@@ -420,19 +514,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
           tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) ys[j * kStageLdH + chl] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          named_bar_sync(2, 128);
+          named_bar_sync(bar_sync, 128);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int idx = i * 128 + ep;
             const int tok = idx >> 4, part = idx & 15;
             const int col = c * 32 + tok;
             const int ch0 = tl.m * 128 + part * 8;
-            if (col < tl.valid && ch0 < P.out_valid_m)
-              *reinterpret_cast<uint4*>(yout + (size_t)(P.out_row_base + tl.row0 + col) * P.out_ld +
-                                        ch0) =
+            if (col < valid && ch0 < P.out_valid_m)
+              *reinterpret_cast<uint4*>(yout + (size_t)(rowb + col) * P.out_ld + ch0) =
                   *reinterpret_cast<const uint4*>(ys + tok * kStageLdH + part * 8);
           }
-          named_bar_sync(2, 128);
+          named_bar_sync(bar_sync, 128);
         }
       } else {
         const int e = tl.m * 128 + q * 32 + lane;
@@ -444,8 +537,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int col = c * 32 + j;
-            if (e_ok && col < tl.valid)
-              lout[(size_t)(tl.row0 + col) * P.out_ld + e] = __uint_as_float(v[j]);
+            if (e_ok && col < valid) lout[(size_t)(rowb + col) * P.out_ld + e] = __uint_as_float(v[j]);
           }
         }
       }
@@ -468,12 +560,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<CG>()) gemm_tc_kernel(co
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc<CG>(tmem_base, tmem_cols<CG>());
+    tmem_dealloc<CG>(tmem_base, tmem_cols<CG, WIDE>());
   }
 }
 
-size_t fixed_smem_bytes(int n_seg) {
-  return 1024 + kBarBytes + kMiscBytes + sizeof(float) * kXchgFloats +
+size_t fixed_smem_bytes(int n_seg, int wide) {
+  return 1024 + kBarBytes + kMiscBytes + sizeof(float) * kXchgFloats * (wide ? 2 : 1) +
          2 * sizeof(int) * (size_t)(n_seg + 1);
 }
 
@@ -492,17 +584,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Opt-in shared memory of a kernel instance, set once per device.
-template <int MODE, int CG>
+template <int MODE, int CG, int WIDE>
 cudaError_t configure(int dev) {
   static std::mutex mu;
   static unsigned long long configured = 0;  // bit per device
   std::lock_guard<std::mutex> g(mu);
   if (dev < 64 && ((configured >> dev) & 1ull)) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(
-      gemm_tc_kernel<MODE, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_limit(CG)));
+  cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel<MODE, CG, WIDE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_limit(CG, WIDE)));
   // the whole unified L1/shared array as shared memory: two pair CTAs per SM need it
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(gemm_tc_kernel<MODE, CG>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    err = cudaFuncSetAttribute(gemm_tc_kernel<MODE, CG, WIDE>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
   if (err == cudaSuccess && dev < 64) configured |= 1ull << dev;
   return err;
@@ -513,15 +607,16 @@ cudaError_t launch_single(const TcParams& p, int sms, size_t smem, cudaStream_t 
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if ((err = configure<MODE, 1>(dev)) != cudaSuccess) return err;
-  gemm_tc_kernel<MODE, 1><<<sms, kThreads, smem, s>>>(p);
+  if ((err = configure<MODE, 1, 0>(dev)) != cudaSuccess) return err;
+  gemm_tc_kernel<MODE, 1, 0><<<sms, threads_of<1, 0>(), smem, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaLaunchConfig_t pair_config(int grid, size_t smem, cudaStream_t s, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t pair_config(int grid, int threads, size_t smem, cudaStream_t s,
+                               cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -539,22 +634,22 @@ cudaLaunchConfig_t pair_config(int grid, size_t smem, cudaStream_t s, cudaLaunch
 // two pairs per TPC measures almost twice the MMA rate of one, so the count is taken from the
 // budget.  Were it ever too high the extra pairs would only wait for a free TPC (the tiles are
 // statically strided over pairs and no pair waits for another), costing time, not results.
-int resident_pairs(int sms, size_t smem) {
-  const int per_sm = smem <= kSmemLimitPair ? ctas_per_sm<2>() : 1;
+int resident_pairs(int sms, size_t smem, int wide) {
+  const int per_sm = !wide && smem <= kSmemLimitPair ? 2 : 1;
   return per_sm * (sms / 2);
 }
 
-template <int MODE>
+template <int MODE, int WIDE>
 cudaError_t launch_pair(const TcParams& p, int sms, size_t smem, cudaStream_t s) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if ((err = configure<MODE, 2>(dev)) != cudaSuccess) return err;
-  const int pairs = resident_pairs(sms, smem);
+  if ((err = configure<MODE, 2, WIDE>(dev)) != cudaSuccess) return err;
+  const int pairs = resident_pairs(sms, smem, WIDE);
   if (pairs < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config(2 * pairs, smem, s, attr);
-  err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, 2>, p);
+  cudaLaunchConfig_t cfg = pair_config(2 * pairs, threads_of<2, WIDE>(), smem, s, attr);
+  err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, 2, WIDE>, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -568,16 +663,21 @@ cudaError_t launch_pair(const TcParams& p, int sms, size_t smem, cudaStream_t s)
 void gemm_tc_plan(int bn, int n_seg, TcParams& p) {
   const int rows = p.cg == 2 ? bn / 2 : bn;
   p.b_stage_bytes = rows * 128;
-  if (p.cg == 2) p.stages_b = bn >= 128 ? 3 : kMaxStagesB;
-  else p.stages_b = bn >= 128 ? 3 : 4;
-  const size_t avail = smem_limit(p.cg) - fixed_smem_bytes(n_seg) - (size_t)p.stages_b * p.b_stage_bytes;
+  const int pa = p.cg == 1 ? producers_a<1, 0>() : (p.wide ? producers_a<2, 1>() : producers_a<2, 0>());
+  const int pb = p.cg == 1 ? producers_b<1, 0>() : (p.wide ? producers_b<2, 1>() : producers_b<2, 0>());
+  if (p.cg == 2 && !p.wide) p.stages_b = bn >= 128 ? 2 : kMaxStagesB;
+  else p.stages_b = bn >= 128 ? (p.wide ? 4 : 3) : 4;
+  p.stages_b -= p.stages_b % pb;
+  const size_t avail = smem_limit(p.cg, p.wide) - fixed_smem_bytes(n_seg, p.wide) -
+                       (size_t)p.stages_b * p.b_stage_bytes;
   int sa = static_cast<int>(avail / kABytes);
-  p.stages_a = sa > kMaxStagesA ? kMaxStagesA : sa;
+  sa = sa > kMaxStagesA ? kMaxStagesA : sa;
+  p.stages_a = sa - sa % pa;
 }
 
 size_t gemm_tc_smem_bytes(const TcParams& p) {
   const int n_seg = p.prob[0].seg_off != nullptr ? p.prob[0].n_seg : 0;
-  size_t b = fixed_smem_bytes(n_seg) + (size_t)p.stages_a * kABytes +
+  size_t b = fixed_smem_bytes(n_seg, p.wide) + (size_t)p.stages_a * kABytes +
              (size_t)p.stages_b * p.b_stage_bytes;
   return p.cg == 1 && b < kSmemFloor ? kSmemFloor : b;
 }
@@ -598,18 +698,21 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 
 cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s) {
   const size_t smem = gemm_tc_smem_bytes(p);
-  if (smem > smem_limit(p.cg) || p.stages_a < 2 || p.stages_b < 2 || p.stages_a > kMaxStagesA ||
-      p.stages_b > kMaxStagesB || (p.cg != 1 && p.cg != 2) || (p.cg == 2 && mode == kModeRouter))
+  const int pa = p.cg == 1 ? producers_a<1, 0>() : (p.wide ? producers_a<2, 1>() : producers_a<2, 0>());
+  const int pb = p.cg == 1 ? producers_b<1, 0>() : (p.wide ? producers_b<2, 1>() : producers_b<2, 0>());
+  if (smem > smem_limit(p.cg, p.wide) || p.stages_a < 2 || p.stages_b < 2 ||
+      p.stages_a > kMaxStagesA || p.stages_b > kMaxStagesB || p.stages_a % pa != 0 ||
+      p.stages_b % pb != 0)
     return cudaErrorInvalidConfiguration;
-  if (p.cg == 2) {
-    if (mode == kModeGateUp) return launch_pair<kModeGateUp>(p, sms, smem, s);
-    return launch_pair<kModeDown>(p, sms, smem, s);
-  }
-  switch (mode) {
-    case kModeRouter: return launch_single<kModeRouter>(p, sms, smem, s);
-    case kModeGateUp: return launch_single<kModeGateUp>(p, sms, smem, s);
-    default: return launch_single<kModeDown>(p, sms, smem, s);
-  }
+  // the forms this library uses: router on one CTA, gate/up on wide pairs, down on pairs
+  if (mode == kModeRouter && p.cg == 1 && !p.wide) return launch_single<kModeRouter>(p, sms, smem, s);
+  if (mode == kModeGateUp && p.cg == 2 && p.wide && p.bn <= 2 * kAccCols)
+    return launch_pair<kModeGateUp, 1>(p, sms, smem, s);
+  if (mode == kModeGateUp && p.cg == 2 && !p.wide && p.bn <= kAccCols)
+    return launch_pair<kModeGateUp, 0>(p, sms, smem, s);
+  if (mode == kModeDown && p.cg == 2 && !p.wide && p.bn <= kAccCols)
+    return launch_pair<kModeDown, 0>(p, sms, smem, s);
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace moe

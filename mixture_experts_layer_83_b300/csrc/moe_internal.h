@@ -55,7 +55,8 @@ struct TcParams {
   TcProblem prob[2];
   int n_prob;
   int cg;             // CTAs per MMA: 1, or 2 (a CTA pair, tcgen05 cta_group::2, M = 256)
-  int bn;             // n-tile cap: multiple of 16, at most 256
+  int wide;           // pairs only: n-tiles up to 512 token rows, split over two MMA issuers
+  int bn;             // n-tile cap: multiple of 16, at most 256 (512 for wide pairs)
   int stages_a;       // depth of the weight ring (16 KiB stages)
   int stages_b;       // depth of the token ring
   int b_stage_bytes;  // B rows one CTA holds per stage (bn, or bn / 2 for a pair) * 128 B
@@ -78,9 +79,10 @@ cudaError_t launch_topk(int src, const float* a, const float* b, const float* bi
                         int k, int* topk_idx, float* topk_w, cudaStream_t s);
 
 // Dispatch (moe_dispatch.cu).
+// ntp / ntp2 (either may be null): n-tile prefixes per expert for n-tile caps bn / bn2.
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
-                            int* expert_counts, int* offsets, int* ntp, int* sorted_token,
-                            int* slot_pos, cudaStream_t s);
+                            int* expert_counts, int* offsets, int* ntp, int bn2, int* ntp2,
+                            int* sorted_token, int* slot_pos, cudaStream_t s);
 cudaError_t launch_gather(const void* x, const int* sorted_token, int R, int d, int elt_bytes,
                           void* xs, cudaStream_t s);
 

@@ -114,10 +114,12 @@ def _check_schedule(s, which, counts):
     tiles, geo = moe.moe_debug_gemm_tiles(s, which, counts)
     assert 2 <= geo["stages_a"] <= 12 and 2 <= geo["stages_b"] <= 8
     assert geo["cg"] == (1 if which == 0 else 2)
-    # one-CTA GEMMs may use the 227 KiB opt-in; pair CTAs share their SM with a second one
-    assert geo["smem_bytes"] <= (232448 if geo["cg"] == 1 else 114688)
+    # one-CTA and wide-pair GEMMs may use the 227 KiB opt-in; narrow pair CTAs share their SM
+    # with a second one
+    assert geo["smem_bytes"] <= (232448 if which == 0 or geo["bn"] > 256 else 114688)
     bn = geo["bn"]
-    assert bn % 16 == 0 and 16 <= bn <= 256
+    # gate/up runs on wide CTA pairs (n-tiles up to 512 token rows), the others up to 256
+    assert bn % 16 == 0 and 16 <= bn <= (512 if which == 1 else 256)
     if which == 0:
         seg_rows = [s.T]
         seg_off = [0, s.T]
@@ -199,8 +201,14 @@ def test_router_gemm_schedule_covers_every_row_once(T, E):
 def test_prefill_geometry_uses_full_width_tiles():
     s = shape(T=8192, d=7168, E=256, k=8, F=2048, Fs=2048)
     _, geo = moe.moe_debug_gemm_tiles(s, 1, np.full(256, 256))
-    assert geo["bn"] == 256 and geo["stages_a"] == 3 and geo["stages_b"] == 3
+    # stage counts are multiples of the producer threads per ring (2 weight, 4 token producers
+    # for the wide gate/up pairs; 2 and 2 for the down pairs)
+    assert geo["bn"] == 512 and geo["stages_a"] == 4 and geo["stages_b"] == 4
     assert geo["m_tiles0"] == 32 and geo["cg"] == 2
+    _, geo = moe.moe_debug_gemm_tiles(s, 2, np.full(256, 256))
+    assert geo["bn"] == 256 and geo["stages_a"] == 4 and geo["stages_b"] == 2
+    assert geo["m_tiles0"] == 56 and geo["cg"] == 2
     _, geo = moe.moe_debug_gemm_tiles(shape(T=128, d=7168, E=256, k=8, F=2048, Fs=2048), 1,
                                       np.full(256, 4))
-    assert geo["bn"] == 32 and geo["stages_a"] == 5 and geo["stages_b"] == 8
+    # decode-sized segments: gate/up on narrow pairs (two per TPC, 112 KiB each)
+    assert geo["bn"] == 32 and geo["stages_a"] == 4 and geo["stages_b"] == 8
