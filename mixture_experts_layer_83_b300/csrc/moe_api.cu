@@ -124,6 +124,11 @@ bool gateup_wide(const moe_shape& s) { return expert_bn(s) >= 256; }
 // n-tile cap of the gate/up GEMM: twice the down GEMM's (512) on wide pairs, the same otherwise.
 int gateup_bn(const moe_shape& s) { return gateup_wide(s) ? 2 * expert_bn(s) : expert_bn(s); }
 
+// The down GEMM (K = F, a short reduction) runs on narrow pairs: its epilogue is a large share
+// of a tile and is hidden by the second pair on the TPC.
+bool down_wide(const moe_shape&) { return false; }
+int down_bn(const moe_shape& s) { return down_wide(s) ? gateup_bn(s) : expert_bn(s); }
+
 // n-tile cap of the router GEMM: about one tile per SM.
 int router_bn(const moe_shape& s, int sms) {
   const int m_tiles = (s.E + 127) / 128;
@@ -211,9 +216,10 @@ void geometry_gateup(const moe_shape& s, TcParams& p) {
 
 void geometry_down(const moe_shape& s, TcParams& p) {
   memset(&p, 0, sizeof(p));
-  const int bn = expert_bn(s);
+  const int bn = down_bn(s);
   p.n_prob = s.Fs > 0 ? 2 : 1;
   p.cg = 2;
+  p.wide = down_wide(s) ? 1 : 0;
   p.bn = bn;
   TcProblem& P = p.prob[0];
   P.a_box_rows = 64;
@@ -288,7 +294,7 @@ int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const voi
   pd.err = status;
   pd.prob[0].out = xs_y;
   pd.prob[0].seg_off = offsets;
-  pd.prob[0].ntp = ntp;
+  pd.prob[0].ntp = down_wide(s) ? ntp2 : ntp;
   if (encode_tmap_bf16(&pd.prob[0].tmA, w_down, (uint64_t)E * d, (uint64_t)F, 64) != 0 ||
       encode_tokens(pd.prob[0], h, R, F) != 0)
     return -1;

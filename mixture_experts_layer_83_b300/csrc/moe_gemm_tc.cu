@@ -712,6 +712,8 @@ cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s)
     return launch_pair<kModeGateUp, 0>(p, sms, smem, s);
   if (mode == kModeDown && p.cg == 2 && !p.wide && p.bn <= kAccCols)
     return launch_pair<kModeDown, 0>(p, sms, smem, s);
+  if (mode == kModeDown && p.cg == 2 && p.wide && p.bn <= 2 * kAccCols)
+    return launch_pair<kModeDown, 1>(p, sms, smem, s);
   return cudaErrorInvalidConfiguration;
 }
 
