@@ -121,8 +121,19 @@ int expert_bn(const moe_shape& s) {
 // two narrow pairs per TPC instead.
 bool gateup_wide(const moe_shape& s) { return expert_bn(s) >= 256; }
 
-// n-tile cap of the gate/up GEMM: twice the down GEMM's (512) on wide pairs, the same otherwise.
-int gateup_bn(const moe_shape& s) { return gateup_wide(s) ? 2 * expert_bn(s) : expert_bn(s); }
+// n-tile cap of the gate/up GEMM on wide pairs: 384 token rows (one pass over an expert's weights
+// for segments up to 384 rows; the cap leaves shared memory for a six-deep weight ring); the
+// down GEMM's cap otherwise.
+int gateup_bn(const moe_shape& s) { return gateup_wide(s) ? 384 : expert_bn(s); }
+
+// Segments of at most 256 rows run on wide pairs as tall tiles: two scheduled m-tiles (512
+// weight rows per pair) over all the segment's rows, one per MMA issuer, which halves the
+// token traffic per FLOP and gives both issuers full-width MMAs.  Needs an even number of
+// scheduled m-tiles.
+int gateup_tall_rows(const moe_shape& s) {
+  const int pairs = (s.F / 64 + 1) / 2;
+  return gateup_wide(s) && pairs % 2 == 0 ? 256 : 0;
+}
 
 // The down GEMM (K = F, a short reduction) runs on narrow pairs: its epilogue is a large share
 // of a tile and is hidden by the second pair on the TPC.
@@ -191,6 +202,7 @@ void geometry_gateup(const moe_shape& s, TcParams& p) {
   P.n_seg = s.E;
   P.K = s.d;
   set_m_tiles(P, s.F / 64, p.cg);
+  P.tall_rows = gateup_tall_rows(s);
   P.a_seg_stride = 2 * s.F;
   P.a_m_stride = 64;
   P.a_box1_off = s.F;
@@ -383,7 +395,8 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                       tidx, tw, stream));
   if (!mark(2)) return MOE_ERR_CUDA;
   MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp,
-                          bf16 ? gateup_bn(S) : 0, bf16 ? ntp2 : nullptr, sorted, slot, stream));
+                          bf16 ? gateup_bn(S) : 0, bf16 ? gateup_tall_rows(S) : 0,
+                          bf16 ? ntp2 : nullptr, sorted, slot, stream));
   if (!mark(3)) return MOE_ERR_CUDA;
   MOE_TRY(launch_gather(x, sorted, R, S.d, bf16 ? 2 : 4, xs_y, stream));
   if (!mark(4)) return MOE_ERR_CUDA;
@@ -473,7 +486,7 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
-                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0,
+                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
                       nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -503,11 +516,11 @@ int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* 
         return MOE_ERR_INVALID_ARG;
       }
       seg[e + 1] = seg[e] + expert_counts[e];
-      ntp[e + 1] = ntp[e] + (expert_counts[e] + p.bn - 1) / p.bn;
+      ntp[e + 1] = ntp[e] + seg_units(expert_counts[e], p.bn, p.prob[0].tall_rows);
     }
     p.prob[0].seg_off = seg;
     p.prob[0].ntp = ntp;
-    tiles0 = ntp[s->E] * p.prob[0].m_tiles;
+    tiles0 = ntp[s->E] * tiles_per_unit(p.prob[0]);
   } else {
     tiles0 = p.prob[0].nt * p.prob[0].m_tiles;
   }
@@ -519,8 +532,10 @@ int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* 
     Tile tl;
     decode_tile(p, seg, ntp, tiles0, t, tl);
     const TcProblem& P = p.prob[tl.prob];
-    for (int r = 0; r < p.cg; ++r) {
-      const int mc = p.cg == 2 ? 2 * tl.m + r : tl.m;
+    for (int x = 0; x < (tl.tall ? 2 : 1) * p.cg; ++x) {
+      const int mp = tl.tall ? 2 * tl.m + x / p.cg : tl.m;  // scheduled m-tile
+      const int r = x % p.cg;
+      const int mc = p.cg == 2 ? 2 * mp + r : mp;
       if (mc >= P.m_cta) continue;
       if (tiles != nullptr && n < max_tiles) {
         int* o = tiles + 7 * (size_t)n;

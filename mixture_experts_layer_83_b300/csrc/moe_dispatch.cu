@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
+#include "tile_sched.h"
 
 namespace moe {
 namespace {
@@ -57,14 +58,15 @@ __device__ int block_inclusive_scan(int v, int* scratch) {
   return v + add;
 }
 
-// ntp / ntp2: prefixes of the n-tiles per expert for n-tile caps bn / bn2 (the two grouped
-// GEMMs tile the token rows differently); either may be null.
+// ntp / ntp2: prefixes of the tile units per expert (seg_units) for n-tile caps bn / bn2 and
+// tall-tile limits 0 / tall2 (the two grouped GEMMs tile the token rows differently); either
+// may be null.
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ chunk_counts,
                                                              int nchunks, int E, int bn,
                                                              int* __restrict__ expert_counts,
                                                              int* __restrict__ offsets,
                                                              int* __restrict__ ntp, int bn2,
-                                                             int* __restrict__ ntp2) {
+                                                             int tall2, int* __restrict__ ntp2) {
   __shared__ int scratch[32];
   const int e = threadIdx.x;
   int tot = 0;
@@ -76,8 +78,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ c
       tot += v;
     }
   }
-  const int nt = (tot + bn - 1) / bn;
-  const int nt2 = bn2 > 0 ? (tot + bn2 - 1) / bn2 : 0;
+  const int nt = seg_units(tot, bn, 0);
+  const int nt2 = bn2 > 0 ? seg_units(tot, bn2, tall2) : 0;
   const int inc_rows = block_inclusive_scan(tot, scratch);
   const int inc_nt = block_inclusive_scan(nt, scratch);
   const int inc_nt2 = block_inclusive_scan(nt2, scratch);
@@ -175,15 +177,15 @@ __global__ void gather_rows_w4_kernel(const uint32_t* __restrict__ x, const int*
 }  // namespace
 
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
-                            int* expert_counts, int* offsets, int* ntp, int bn2, int* ntp2,
-                            int* sorted_token, int* slot_pos, cudaStream_t s) {
+                            int* expert_counts, int* offsets, int* ntp, int bn2, int tall2,
+                            int* ntp2, int* sorted_token, int* slot_pos, cudaStream_t s) {
   const int R = T * k;
   const int nchunks = (R + kDispatchChunk - 1) / kDispatchChunk;
   dispatch_count_kernel<<<nchunks, 256, E * sizeof(int), s>>>(topk_idx, R, E, chunk_counts);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, bn, expert_counts, offsets, ntp,
-                                          bn2, ntp2);
+                                          bn2, tall2, ntp2);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scatter_kernel<<<nchunks, kDispatchWarps * 32, kDispatchWarps * E * sizeof(int), s>>>(

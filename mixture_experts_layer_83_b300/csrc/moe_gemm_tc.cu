@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
   tc_fence_after();
   const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
 
-  const int tiles0 = (n_seg0 > 0 ? s_ntp[n_seg0] : p.prob[0].nt) * p.prob[0].m_tiles;
+  const int tiles0 = n_seg0 > 0 ? s_ntp[n_seg0] * tiles_per_unit(p.prob[0])
+                                : p.prob[0].nt * p.prob[0].m_tiles;
   const int tiles1 = p.n_prob > 1 ? p.prob[1].nt * p.prob[1].m_tiles : 0;
   const int total = tiles0 + tiles1;
 
@@ -251,42 +252,47 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
         Tile tl;
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
-        const int mc = CG == 2 ? 2 * tl.m + rank : tl.m;
-        const int arow = tl.seg * P.a_seg_stride + mc * P.a_m_stride;
-        const bool box1 = a_has_box1(P, mc);
         const uint64_t pol = tl.nt > 1 ? pol_shared : pol_once;
-        // the even CTA's barrier counts the bytes of both CTAs of a pair
-        const uint32_t bytes = CG == 2 ? a_block_bytes(P, 2 * tl.m) + a_block_bytes(P, 2 * tl.m + 1)
-                                       : a_block_bytes(P, mc);
+        // a tall tile's k-step fills two weight stages, one per scheduled m-tile (and issuer)
+        const int parts = tl.tall ? 2 : 1;
         const int kblocks = P.K >> 6;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (stage % kProdA != pid) {  // another producer's stage
+        for (int kb = 0; kb < kblocks && ok; ++kb) {
+          for (int part = 0; part < parts; ++part) {
+            if (stage % kProdA != pid) {  // another producer's stage
+              if (++stage == SA) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
+            const int mp = tl.tall ? 2 * tl.m + part : tl.m;  // scheduled m-tile
+            const int mc = CG == 2 ? 2 * mp + rank : mp;        // this CTA's weight tile
+            const int arow = tl.seg * P.a_seg_stride + mc * P.a_m_stride;
+            const bool box1 = a_has_box1(P, mc);
+            // the even CTA's barrier counts the bytes of both CTAs of a pair
+            const uint32_t bytes = CG == 2 ? a_block_bytes(P, 2 * mp) + a_block_bytes(P, 2 * mp + 1)
+                                           : a_block_bytes(P, mc);
+            if (!mbar_wait(&empty_a[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sA = ring_a + (size_t)stage * kABytes;
+            if (leader) {
+              mbar_arrive_expect_tx(&full_a[stage], bytes);
+              ++armed[stage];
+            }
+            if constexpr (CG == 2) {
+              const uint32_t fb = mapa_shared(smem_u32(&full_a[stage]), 0);
+              tma_load_2d_pair(sA, &P.tmA, fb, kb * 64, arow, pol);
+              if (box1) tma_load_2d_pair(sA + 64 * 128, &P.tmA, fb, kb * 64, arow + P.a_box1_off, pol);
+            } else {
+              tma_load_2d(sA, &P.tmA, &full_a[stage], kb * 64, arow, pol);
+              if (box1) tma_load_2d(sA + 64 * 128, &P.tmA, &full_a[stage], kb * 64, arow + P.a_box1_off, pol);
+            }
             if (++stage == SA) {
               stage = 0;
               phase ^= 1u;
             }
-            continue;
-          }
-          if (!mbar_wait(&empty_a[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sA = ring_a + (size_t)stage * kABytes;
-          if (leader) {
-            mbar_arrive_expect_tx(&full_a[stage], bytes);
-            ++armed[stage];
-          }
-          if constexpr (CG == 2) {
-            const uint32_t fb = mapa_shared(smem_u32(&full_a[stage]), 0);
-            tma_load_2d_pair(sA, &P.tmA, fb, kb * 64, arow, pol);
-            if (box1) tma_load_2d_pair(sA + 64 * 128, &P.tmA, fb, kb * 64, arow + P.a_box1_off, pol);
-          } else {
-            tma_load_2d(sA, &P.tmA, &full_a[stage], kb * 64, arow, pol);
-            if (box1) tma_load_2d(sA + 64 * 128, &P.tmA, &full_a[stage], kb * 64, arow + P.a_box1_off, pol);
-          }
-          if (++stage == SA) {
-            stage = 0;
-            phase ^= 1u;
           }
         }
       }
@@ -377,8 +383,11 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
         decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
         const TcProblem& P = p.prob[tl.prob];
         const NSplit ns = n_split<WIDE>(tl.ncols);
-        const int nh = h == 0 ? ns.n0 : ns.n1;
-        const int brow = h == 0 ? 0 : (CG == 2 ? ns.n0 >> 1 : ns.n0);  // stage row of this MMA's B
+        // a wide tile splits its token columns over the issuers; a tall tile gives each issuer
+        // all of them against its own weight stage
+        const int nh = tl.tall ? tl.ncols : (h == 0 ? ns.n0 : ns.n1);
+        const int brow = tl.tall || h == 0 ? 0 : (CG == 2 ? ns.n0 >> 1 : ns.n0);  // B stage row
+        const int parts = tl.tall ? 2 : 1;
         const int buf = acc_i % kBufs;
         const uint32_t use = static_cast<uint32_t>(acc_i / kBufs);
         // a pair's accumulator is free once the epilogues of both CTAs have read it
@@ -391,26 +400,35 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
         const uint32_t idesc = idesc_bf16_f32(128 * CG, nh > 0 ? nh : 16);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&full_a[sa], pa, abort_flag, p.err, kErrMmaWait) ||
-              !mbar_wait(&full_b[sb], pb, abort_flag, p.err, kErrMmaWait)) {
+          // every issuer waits for every stage of the k-step and releases each of them
+          int ast[2];
+          uint32_t aph[2];
+          for (int x = 0; x < parts; ++x) {
+            ast[x] = sa;
+            aph[x] = pa;
+            if (++sa == SA) {
+              sa = 0;
+              pa ^= 1u;
+            }
+          }
+          bool got = mbar_wait(&full_b[sb], pb, abort_flag, p.err, kErrMmaWait);
+          for (int x = 0; x < parts && got; ++x)
+            got = mbar_wait(&full_a[ast[x]], aph[x], abort_flag, p.err, kErrMmaWait);
+          if (!got) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (nh > 0) {
-            const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)sa * kABytes));
+            const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)ast[tl.tall ? h : 0] * kABytes));
             const uint64_t bd =
                 sdesc_k_sw128(smem_u32(ring_b + (size_t)sb * p.b_stage_bytes + (size_t)brow * 128));
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mma_bf16<CG>(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
           }
-          mma_commit<CG>(&empty_a[sa]);
+          for (int x = 0; x < parts; ++x) mma_commit<CG>(&empty_a[ast[x]]);
           mma_commit<CG>(&empty_b[sb]);
-          if (++sa == SA) {
-            sa = 0;
-            pa ^= 1u;
-          }
           if (++sb == SB) {
             sb = 0;
             pb ^= 1u;
@@ -442,7 +460,10 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
       Tile tl;
       decode_tile(p, s_seg, s_ntp, tiles0, t, tl);
       const TcProblem& P = p.prob[tl.prob];
-      if (CG == 2) tl.m = 2 * tl.m + rank;  // this CTA's 128-row weight tile
+      // this group's scheduled m-tile (a tall tile's group g takes the g-th of its two) and this
+      // CTA's 128-row weight tile within it
+      const int mp = tl.tall ? 2 * tl.m + g : tl.m;
+      tl.m = CG == 2 ? 2 * mp + rank : mp;
       const NSplit ns = n_split<WIDE>(tl.ncols);
       const int buf = acc_i % kBufs;
       const uint32_t use = static_cast<uint32_t>(acc_i / kBufs);
@@ -451,8 +472,8 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
       if (named_bar_or(bar_or, 128, !ok || *abort_flag != 0)) break;
       tc_fence_after();
       // this group's token columns: [c0, c0 + valid) of the tile, at accumulator column acol
-      const int c0 = g == 0 ? 0 : ns.n0;
-      const int width = g == 0 ? ns.n0 : ns.n1;
+      const int c0 = tl.tall || g == 0 ? 0 : ns.n0;
+      const int width = tl.tall ? tl.ncols : (g == 0 ? ns.n0 : ns.n1);
       int valid = tl.valid - c0;
       valid = valid < 0 ? 0 : (valid > width ? width : valid);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +

@@ -33,7 +33,8 @@ struct TcProblem {
   CUtensorMap tmB[5];  // tokens  [rows][K]: boxes of 128 / 64 / 32 / 16 / 8 rows x 64 columns
   void* out;
   const int* seg_off;  // grouped: device [n_seg+1] first B row of each segment; null = single
-  const int* ntp;      // grouped: device [n_seg+1] prefix of n-tiles per segment
+  const int* ntp;      // grouped: device [n_seg+1] prefix of tile units per segment
+  int tall_rows;       // grouped, pairs: segments of 1..tall_rows rows run as tall tiles (0: none)
   int K;               // reduction length, multiple of 64
   int m_tiles;         // scheduled m-tiles per segment: weight tiles of one CTA, or of a pair
   int m_cta;           // 128-row weight tiles per segment (a pair's second tile may be past it)
@@ -79,10 +80,11 @@ cudaError_t launch_topk(int src, const float* a, const float* b, const float* bi
                         int k, int* topk_idx, float* topk_w, cudaStream_t s);
 
 // Dispatch (moe_dispatch.cu).
-// ntp / ntp2 (either may be null): n-tile prefixes per expert for n-tile caps bn / bn2.
+// ntp / ntp2 (either may be null): per-expert prefixes of tile units (seg_units) for n-tile
+// caps bn / bn2 and tall-tile limits 0 / tall2.
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
-                            int* expert_counts, int* offsets, int* ntp, int bn2, int* ntp2,
-                            int* sorted_token, int* slot_pos, cudaStream_t s);
+                            int* expert_counts, int* offsets, int* ntp, int bn2, int tall2,
+                            int* ntp2, int* sorted_token, int* slot_pos, cudaStream_t s);
 cudaError_t launch_gather(const void* x, const int* sorted_token, int R, int d, int elt_bytes,
                           void* xs, cudaStream_t s);
 

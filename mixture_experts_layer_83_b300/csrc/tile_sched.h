@@ -12,10 +12,27 @@
 
 namespace moe {
 
+// Tile units of a segment of n rows with n-tile cap bn: a segment of 1..tall_rows rows is one
+// unit (a tall tile per two scheduled m-tiles); otherwise each of its ceil(n / bn) n-tiles is
+// one unit per scheduled m-tile, counted twice when tall tiles exist so that a unit is always
+// worth (m_tiles / 2) tiles.
+MOE_HD int seg_units(int n, int bn, int tall_rows) {
+  if (n <= 0) return 0;
+  if (tall_rows > 0 && n <= tall_rows) return 1;
+  return (tall_rows > 0 ? 2 : 1) * ((n + bn - 1) / bn);
+}
+
+// Tiles per unit of a grouped operand set.
+MOE_HD int tiles_per_unit(const TcProblem& P) {
+  return P.tall_rows > 0 ? P.m_tiles / 2 : P.m_tiles;
+}
+
 struct Tile {
   int prob;   // 0 = first operand set (grouped or single), 1 = second (single)
   int seg;    // segment (expert) within the operand set
-  int m;      // scheduled m-tile within the segment (a pair's tiles are 2m and 2m + 1)
+  int m;      // scheduled m-tile within the segment (a pair's tiles are 2m and 2m + 1); for a
+              // tall tile, the pair of scheduled m-tiles 2m and 2m + 1
+  int tall;   // 1: a tall tile (two scheduled m-tiles over the whole segment, one per issuer)
   int row0;   // first B row of the tile
   int ncols;  // MMA N: multiple of 16, at most the n-tile cap
   int valid;  // B rows of the tile that belong to the segment (<= ncols)
@@ -26,8 +43,9 @@ struct Tile {
 // segment tiles run in (m-group, m, n-tile) order: the n-tiles that share a weight tile are
 // neighbours in the schedule (and so run at the same time on neighbouring CTAs, sharing the
 // weight tile through L2), and a group of m-tiles shares each token tile.  A segment of n
-// rows is cut into nt n-tiles of whole 16-row units, as even as possible.  `seg_off` / `ntp`
-// are the segment row offsets and the n-tile prefix of set 0 when it is grouped.
+// rows is cut into nt n-tiles of whole 16-row units, as even as possible.  A segment of at
+// most tall_rows rows instead runs as m_tiles / 2 tall tiles over all its rows.  `seg_off` /
+// `ntp` are the segment row offsets and the unit prefix of set 0 when it is grouped.
 MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, int tiles0, int t,
                         Tile& tl) {
   int prob = 0, local = t;
@@ -36,10 +54,11 @@ MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, i
     local = t - tiles0;
   }
   const TcProblem& P = p.prob[prob];
-  const int M = P.m_tiles;
   int seg = 0, nt, seg_row0 = 0, seg_rows;
+  tl.tall = 0;
   if (prob == 0 && P.seg_off != nullptr) {
-    const int q = local / M;
+    const int tpu = tiles_per_unit(P);
+    const int q = local / tpu;
     int lo = 0, hi = P.n_seg;  // largest lo with ntp[lo] <= q
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -47,10 +66,22 @@ MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, i
       else hi = mid;
     }
     seg = lo;
-    nt = ntp[seg + 1] - ntp[seg];
-    local -= ntp[seg] * M;
+    const int units = ntp[seg + 1] - ntp[seg];
+    local -= ntp[seg] * tpu;
     seg_row0 = seg_off[seg];
     seg_rows = seg_off[seg + 1] - seg_row0;
+    if (P.tall_rows > 0 && units == 1) {
+      tl.prob = prob;
+      tl.seg = seg;
+      tl.m = local;
+      tl.tall = 1;
+      tl.nt = 1;
+      tl.row0 = seg_row0;
+      tl.ncols = ((seg_rows + 15) >> 4) << 4;
+      tl.valid = seg_rows;
+      return;
+    }
+    nt = P.tall_rows > 0 ? units >> 1 : units;
   } else {
     nt = P.nt;
     seg_rows = P.rows;

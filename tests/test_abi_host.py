@@ -203,7 +203,7 @@ def test_prefill_geometry_uses_full_width_tiles():
     _, geo = moe.moe_debug_gemm_tiles(s, 1, np.full(256, 256))
     # stage counts are multiples of the producer threads per ring (2 weight, 4 token producers
     # for the wide gate/up pairs; 2 and 2 for the down pairs)
-    assert geo["bn"] == 512 and geo["stages_a"] == 4 and geo["stages_b"] == 4
+    assert geo["bn"] == 384 and geo["stages_a"] == 6 and geo["stages_b"] == 4
     assert geo["m_tiles0"] == 32 and geo["cg"] == 2
     _, geo = moe.moe_debug_gemm_tiles(s, 2, np.full(256, 256))
     assert geo["bn"] == 256 and geo["stages_a"] == 4 and geo["stages_b"] == 2
@@ -212,3 +212,25 @@ def test_prefill_geometry_uses_full_width_tiles():
                                       np.full(256, 4))
     # decode-sized segments: gate/up on narrow pairs (two per TPC, 112 KiB each)
     assert geo["bn"] == 32 and geo["stages_a"] == 4 and geo["stages_b"] == 8
+
+
+def test_gateup_tall_and_wide_tiles():
+    """Prefill gate/up: segments of up to 256 rows run as tall tiles (four weight tiles of 128
+    rows, i.e. two pairs, over all the segment's rows); longer ones as wide tiles (one pair over
+    up to 384 rows)."""
+    s = shape(T=8192, d=7168, E=256, k=8, F=2048, Fs=2048)
+    counts = np.full(256, 256)
+    counts[1] = 300
+    counts[2] = 0
+    counts[3] = 10
+    tiles, geo = moe.moe_debug_gemm_tiles(s, 1, counts)
+    routed = tiles[tiles[:, 0] == 0]
+    for e, n in ((0, 256), (1, 300), (3, 10)):
+        t = routed[routed[:, 1] == e]
+        assert len(t) == 32 and sorted(t[:, 2].tolist()) == list(range(32))
+        assert (t[:, 5] == n).all() and (t[:, 4] == (n + 15) // 16 * 16).all()
+        if n <= 256:   # tall: the CTA tiles of one tile are four consecutive weight tiles
+            assert (t[:, 2].reshape(-1, 4) == t[::4, 2:3] + np.arange(4)).all()
+        else:          # wide: two consecutive weight tiles (a pair)
+            assert (t[:, 2].reshape(-1, 2) == t[::2, 2:3] + np.arange(2)).all()
+    assert (routed[:, 1] != 2).all()
