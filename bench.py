@@ -213,33 +213,62 @@ class Runner:
         return ms, stages, (t0, t1)
 
     def timed_e2e(self, steps, warmup, world):
-        """Host (pinned) x -> device, forward, device out + counts -> host, every step."""
+        """End to end through the public entry point, every step: pinned host x -> device,
+        forward, device out + expert counts -> pinned host.  Copies run on their own streams,
+        double-buffered, so step i+1's upload and step i-1's read-back overlap step i; the timed
+        region spans the first upload to the last read-back."""
         torch = self.torch
         x_host = self.dev["x"].cpu().pin_memory()
-        out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        cnt_host = torch.empty(self.counts.shape, dtype=torch.int32).pin_memory()
-        x_dev = torch.empty_like(self.dev["x"])
+        nbuf = 2
+        x_dev = [torch.empty_like(self.dev["x"]) for _ in range(nbuf)]
+        out_dev = [torch.empty_like(self.out) for _ in range(nbuf)]
+        cnt_dev = [torch.empty_like(self.counts) for _ in range(nbuf)]
+        out_host = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory() for _ in range(nbuf)]
+        cnt_host = [torch.empty(self.counts.shape, dtype=torch.int32).pin_memory() for _ in range(nbuf)]
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        comp = self.stream
+        uploaded = [torch.cuda.Event() for _ in range(nbuf)]
+        computed = [torch.cuda.Event() for _ in range(nbuf)]
+        consumed = [torch.cuda.Event() for _ in range(nbuf)]   # x buffer free again
+        read_back = [torch.cuda.Event() for _ in range(nbuf)]  # out buffer free again
+        for e in consumed + read_back:
+            e.record(comp)
 
-        def one():
-            x_dev.copy_(x_host, non_blocking=True)
-            self.step(x=x_dev)
-            out_host.copy_(self.out, non_blocking=True)
-            cnt_host.copy_(self.counts, non_blocking=True)
+        def run(n):
+            for i in range(n):
+                b = i % nbuf
+                with torch.cuda.stream(up):
+                    up.wait_event(consumed[b])
+                    x_dev[b].copy_(x_host, non_blocking=True)
+                    uploaded[b].record(up)
+                comp.wait_event(uploaded[b])
+                comp.wait_event(read_back[b])
+                self.moe.moe_layer_forward(self.shape, x_dev[b], self.dev["w_router"],
+                                           self.dev["w_gate_up"], self.dev["w_down"],
+                                           self.c["score"], self.dev.get("bias"), self.shared,
+                                           out_dev[b], cnt_dev[b], self.ws, self.ws_bytes, comp)
+                consumed[b].record(comp)
+                computed[b].record(comp)
+                with torch.cuda.stream(down):
+                    down.wait_event(computed[b])
+                    out_host[b].copy_(out_dev[b], non_blocking=True)
+                    cnt_host[b].copy_(cnt_dev[b], non_blocking=True)
+                    read_back[b].record(down)
 
-        for _ in range(warmup):
-            one()
+        run(warmup)
         torch.cuda.synchronize()
         barrier(world)
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(self.stream)
-        for _ in range(steps):
-            one()
-        stop.record(self.stream)
+        start.record(up)
+        run(steps)
+        down.wait_stream(up)
+        down.wait_stream(comp)
+        stop.record(down)
         torch.cuda.synchronize()
         barrier(world)
         ms = start.elapsed_time(stop) / steps
         h2d = x_host.numel() * x_host.element_size()
-        d2h = out_host.numel() * out_host.element_size() + cnt_host.numel() * 4
+        d2h = out_host[0].numel() * out_host[0].element_size() + cnt_host[0].numel() * 4
         return ms, h2d, d2h
 
 
@@ -341,12 +370,19 @@ def measure(c, args, world, rank, peaks, sampler, kind):
            "runner": r, "dev": dev}
     fl = layer_flops(c)
     by = layer_bytes(c, counts)
-    t_roof = max(fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
+    # The layer runs as back-to-back passes (a long step under the power cap), so compute is
+    # bounded by the sustained bf16 figure; the burst-based roofline is reported beside it.
+    t_mem = by / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(fl / (peaks["bf16_tflops_sustained"] * 1e12), t_mem)
+    t_roof_burst = max(fl / (peaks["bf16_tflops"] * 1e12), t_mem)
     res["layer"] = {"tflops": fl / (ms_max * 1e-3) / 1e12, "gbs": by / (ms_max * 1e-3) / 1e9,
                     "flop": fl, "bytes": by, "roofline_ms": t_roof * 1e3,
                     "roofline_frac": t_roof * 1e3 / ms_max,
-                    "bound": "tensor" if fl / (peaks["bf16_tflops"] * 1e12) >=
-                    by / (peaks["hbm_gbs"] * 1e9) else "hbm"}
+                    "roofline_ms_burst": t_roof_burst * 1e3,
+                    "roofline_frac_burst": t_roof_burst * 1e3 / ms_max,
+                    "roofline_peaks": "bf16 sustained (burst beside it) and HBM copy, measured",
+                    "bound": "tensor" if fl / (peaks["bf16_tflops_sustained"] * 1e12) >= t_mem
+                    else "hbm"}
     return res
 
 
@@ -416,11 +452,15 @@ def main():
     gu_fl = gateup_flops(c)
     achieved = gu_fl / (gu_ms * 1e-3) / 1e12
     traffic = traffic_record("gemm_gateup_prefill")
-    roof = {"kernel": "gemm_tc_kernel<gate/up+SwiGLU> (tcgen05)", "bound": "tensor",
-            "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
-            "peak_source": f"{peak_src} bf16 burst",
-            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+    # the gate/up GEMM is timed inside a long step (the timed passes run back to back under
+    # the power cap): its peak is the sustained bf16 figure; the burst fraction is beside it
+    roof = {"kernel": "gemm_tc_kernel<1,2,1> gate/up + SwiGLU (tcgen05, wide CTA pairs)",
+            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
+            "traffic": traffic,
+            "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step of "
+                           f"{args.steps} back-to-back passes)",
+            "frac_of_burst": achieved / peaks["bf16_tflops"], "burst_peak": peaks["bf16_tflops"],
             "algorithmic_flop_per_launch": gu_fl, "ms_per_launch": gu_ms}
     clocks = sampler.summary(min(main_res["t0"], dec["t0"]), max(main_res["t1"], dec["t1"]))
 
@@ -432,7 +472,8 @@ def main():
     decode = {"workload": workload_config(dc)["workload"], "value": dc["T"] * world / (dms * 1e-3),
               "unit": "tokens/s", "ms_per_step": dms, "layer": dec["layer"],
               "stages_ms": {n: float(v) for n, v in zip(names, dst)},
-              "roofline": {"kernel": "gemm_tc_kernel<gate/up+SwiGLU> (tcgen05)", "bound": "hbm",
+              "roofline": {"kernel": "gemm_tc_kernel<1,2,0> gate/up + SwiGLU (tcgen05, narrow CTA "
+                                     "pairs)", "bound": "hbm",
                            "achieved": d_gu_bytes / (d_gu_ms * 1e-3) / 1e9,
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": d_gu_bytes / (d_gu_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -455,7 +496,9 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(c),
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copies": "pinned host buffers, every step; uploads and read-backs on their own "
+                          "streams, double-buffered, overlapping the neighbouring steps' compute"},
         "gpu_launches": int(r_launches(c) * args.steps),
         "clocks": clocks,
         "layer": main_res["layer"],
