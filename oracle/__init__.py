@@ -54,12 +54,14 @@ def lib():
         l.oracle_elem.restype = ctypes.c_double
         l.oracle_router_scores.argtypes = [ci, ci, ci, ci, vp, vp, ci, vp, vp, vp, vp]
         l.oracle_topk.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
+        l.oracle_topk_grouped.argtypes = [ci, ci, ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_dispatch.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_gather.argtypes = [ci, ci, vp, vp, vp]
         l.oracle_combine.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_swiglu_ffn.argtypes = [ci, ci, ci, vp, vp, vp, vp]
         l.oracle_layer_rows.argtypes = [ctypes.POINTER(OracleLayer), ci, vp, vp, vp, vp]
-        for f in ("oracle_router_scores", "oracle_topk", "oracle_dispatch", "oracle_gather",
+        for f in ("oracle_router_scores", "oracle_topk", "oracle_topk_grouped", "oracle_dispatch",
+                  "oracle_gather",
                   "oracle_combine", "oracle_swiglu_ffn", "oracle_layer_rows"):
             getattr(l, f).restype = ci
         _lib = l
@@ -103,6 +105,17 @@ def topk(key, score, k):
     n, E = key.shape
     idx = np.empty((n, k), dtype=np.int32); w = np.empty((n, k)); margin = np.empty(n)
     _check(lib().oracle_topk(n, E, k, _p(key), _p(score), _p(idx), _p(w), _p(margin)), "topk")
+    return idx, w, margin
+
+
+def topk_grouped(key, score, k, n_groups, topk_groups):
+    """Group-limited top-k (see moe_oracle.h): (topk_idx, topk_w, margin)."""
+    key = np.ascontiguousarray(key, dtype=np.float64)
+    score = np.ascontiguousarray(score, dtype=np.float64)
+    n, E = key.shape
+    idx = np.empty((n, k), dtype=np.int32); w = np.empty((n, k)); margin = np.empty(n)
+    _check(lib().oracle_topk_grouped(n, E, k, n_groups, topk_groups, _p(key), _p(score), _p(idx),
+                                     _p(w), _p(margin)), "topk_grouped")
     return idx, w, margin
 
 

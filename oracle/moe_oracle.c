@@ -101,6 +101,86 @@ int oracle_topk(int n_tok, int E, int k, const double* key, const double* score,
   return 0;
 }
 
+/* Group-limited (node-limited) top-k.  Page "Expert-Parallel MoE Inference: Serving Sparse
+ * Models at Scale", section "Load imbalance and how to fight it": node-limited routing caps how
+ * many nodes (groups of experts) a token's experts may span.  The experts form n_groups
+ * contiguous groups of E / n_groups.  The pages do not say how a group is scored; the reading
+ * taken here: a group's score is the largest key among its experts.  The topk_groups groups
+ * with the largest scores are kept (equal scores: the lower group id), then the top-k is taken
+ * as in oracle_topk over the experts of the kept groups only, and renormalised the same way. */
+int oracle_topk_grouped(int n_tok, int E, int k, int n_groups, int topk_groups,
+                        const double* key, const double* score, int* topk_idx, double* topk_w,
+                        double* margin) {
+  if (n_tok < 0 || E < 1 || k < 1 || k > E || !key || !topk_idx) return -1;
+  if (n_groups < 1 || E % n_groups != 0 || topk_groups < 1 || topk_groups > n_groups) return -1;
+  const int gsize = E / n_groups;
+  if (topk_groups * gsize < k) return -1;
+  if (topk_w && !score) return -1;
+  char* taken = (char*)malloc((size_t)E);
+  char* allowed = (char*)malloc((size_t)E);
+  char* gsel = (char*)malloc((size_t)n_groups);
+  double* gscore = (double*)malloc(sizeof(double) * (size_t)n_groups);
+  if (!taken || !allowed || !gsel || !gscore) {
+    free(taken); free(allowed); free(gsel); free(gscore);
+    return -1;
+  }
+  for (int t = 0; t < n_tok; ++t) {
+    const double* kr = key + (size_t)t * E;
+    /* group scores: the best key of each group */
+    for (int g = 0; g < n_groups; ++g) {
+      double best = kr[g * gsize];
+      for (int i = 1; i < gsize; ++i)
+        if (kr[g * gsize + i] > best) best = kr[g * gsize + i];
+      gscore[g] = best;
+    }
+    /* keep topk_groups groups: each time the unkept group with the largest score */
+    memset(gsel, 0, (size_t)n_groups);
+    int last_kept = -1;
+    for (int r = 0; r < topk_groups; ++r) {
+      int bg = -1;
+      for (int g = 0; g < n_groups; ++g) {
+        if (gsel[g]) continue;
+        if (bg < 0 || gscore[g] > gscore[bg]) bg = g;
+      }
+      gsel[bg] = 1;
+      last_kept = bg;
+    }
+    double gmargin = INFINITY;
+    for (int g = 0; g < n_groups; ++g)
+      if (!gsel[g] && gscore[last_kept] - gscore[g] < gmargin) gmargin = gscore[last_kept] - gscore[g];
+    for (int e = 0; e < E; ++e) allowed[e] = gsel[e / gsize];
+    /* top-k over the allowed experts */
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (!allowed[e] || taken[e]) continue;
+        if (best < 0 || kr[e] > kr[best]) best = e;
+      }
+      taken[best] = 1;
+      topk_idx[(size_t)t * k + j] = best;
+    }
+    if (margin) {
+      int next = -1;
+      for (int e = 0; e < E; ++e)
+        if (allowed[e] && !taken[e] && (next < 0 || kr[e] > kr[next])) next = e;
+      const double emargin = next < 0 ? INFINITY : kr[topk_idx[(size_t)t * k + k - 1]] - kr[next];
+      margin[t] = emargin < gmargin ? emargin : gmargin;
+    }
+    if (topk_w) {
+      const double* sr = score + (size_t)t * E;
+      double den = 0.0;
+      for (int j = 0; j < k; ++j) den += sr[topk_idx[(size_t)t * k + j]];
+      for (int j = 0; j < k; ++j) topk_w[(size_t)t * k + j] = sr[topk_idx[(size_t)t * k + j]] / den;
+    }
+  }
+  free(taken);
+  free(allowed);
+  free(gsel);
+  free(gscore);
+  return 0;
+}
+
 /* Group the (token, slot) assignments by expert, token order preserved within an expert:
  * the single-GPU form of the dispatch all-to-all (page "Expert-Parallel MoE Inference",
  * "The all-to-all dispatch and combine, step by step"; page "MoE Expert Parallelism in

@@ -58,6 +58,15 @@ int oracle_router_scores(int n_tok, int d, int E, int dtype, const void* x_rows,
 int oracle_topk(int n_tok, int E, int k, const double* key, const double* score,
                 int* topk_idx, double* topk_w, double* margin);
 
+/* Group-limited top-k: experts in n_groups contiguous groups of E / n_groups; a group's score
+ * is its largest key; the topk_groups best groups are kept (ties -> lower group id); the top-k
+ * and renormalisation of oracle_topk then run over the kept groups' experts only.
+ * margin [n_tok] = min(topk_groups-th group score minus the next group's, k-th key minus the
+ * (k+1)-th key among the kept experts), +inf where there is no next. */
+int oracle_topk_grouped(int n_tok, int E, int k, int n_groups, int topk_groups,
+                        const double* key, const double* score, int* topk_idx, double* topk_w,
+                        double* margin);
+
 /* Dispatch tables of a routing (topk_idx [T][k]):
  *   counts[e] = number of tokens routed to e; offsets = exclusive prefix sum (E+1 entries);
  *   sorted_token[R] (R = T*k): for e = 0..E-1, the tokens routed to e in ascending order;

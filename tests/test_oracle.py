@@ -149,6 +149,81 @@ def test_topk_brute_force_with_ties(E, k):
             assert margin[t] == np.inf
 
 
+# ------------------------------------------------------------------ group-limited top-k
+def test_hand_case_group_limited_routing():
+    """E=8 in 4 groups of 2, keep 2 groups, k=3; keys [0.9,0.1 | 0.2,0.15 | 0.85,0.8 | 0.3,0.95].
+    Group scores (best key): 0.9, 0.2, 0.85, 0.95 -> groups 3 and 0 kept -> experts {0,1,6,7};
+    top-3 by key: 7 (0.95), 0 (0.9), 6 (0.3).  Plain top-3 would take 4 (0.85) instead of 6.
+    Catches: group scored by its mean or sum (sum keeps group 2), groups not limiting the choice."""
+    key = np.array([[0.9, 0.1, 0.2, 0.15, 0.85, 0.8, 0.3, 0.95]])
+    idx, w, margin = oracle.topk_grouped(key, key, 3, 4, 2)
+    assert idx[0].tolist() == [7, 0, 6]
+    np.testing.assert_allclose(w[0], np.array([0.95, 0.9, 0.3]) / 2.15, rtol=1e-15)
+    # margins: kept groups' 2nd score 0.9 vs the best dropped 0.85 -> 0.05; experts: 0.3 vs 0.1
+    assert margin[0] == pytest.approx(0.05, abs=1e-15)
+    pidx, _, _ = oracle.topk(key, key, 3)
+    assert pidx[0].tolist() == [7, 0, 4]
+
+
+def test_group_limited_tie_breaks_to_lower_group():
+    """Two groups with equal best keys and room for one: the lower group id is kept."""
+    key = np.array([[0.5, 0.1, 0.5, 0.4, 0.2, 0.3]])   # 3 groups of 2, best keys 0.5, 0.5, 0.3
+    idx, _, margin = oracle.topk_grouped(key, key, 2, 3, 1)
+    assert idx[0].tolist() == [0, 1] and margin[0] == 0.0
+
+
+@pytest.mark.parametrize("E,G,M,k", [(8, 4, 2, 3), (8, 2, 1, 4), (9, 3, 2, 4), (12, 4, 3, 5),
+                                     (10, 5, 2, 2), (12, 6, 6, 6), (8, 8, 3, 3)])
+def test_group_limited_brute_force_with_ties(E, G, M, k):
+    """Against brute force: enumerate every set of M groups and every k-subset of their experts;
+    the chosen groups are the unique M-set whose every member beats every non-member by group
+    score (best key; ties -> lower group id), and the chosen experts the unique k-subset of the
+    kept experts whose members beat every other kept expert.  Quantised keys make ties common."""
+    rng = np.random.default_rng(E * 101 + G * 7 + M * 3 + k)
+    key = np.round(rng.standard_normal((150, E)) * 2) / 2
+    score = rng.uniform(0.1, 1.0, (150, E))
+    idx, w, margin = oracle.topk_grouped(key, score, k, G, M)
+    gs = E // G
+
+    def beats(a, b, v):
+        return v[a] > v[b] or (v[a] == v[b] and a < b)
+
+    for t in range(150):
+        kr = key[t]
+        gscore = [max(kr[g * gs:(g + 1) * gs]) for g in range(G)]
+        gsets = [S for S in itertools.combinations(range(G), M)
+                 if all(beats(a, b, gscore) for a in S for b in range(G) if b not in S)]
+        assert len(gsets) == 1
+        allowed = [e for e in range(E) if e // gs in gsets[0]]
+        esets = [S for S in itertools.combinations(allowed, k)
+                 if all(beats(a, b, kr) for a in S for b in allowed if b not in S)]
+        assert len(esets) == 1
+        order = sorted(esets[0], key=lambda e: (-kr[e], e))
+        assert idx[t].tolist() == order
+        sel = score[t, order]
+        np.testing.assert_allclose(w[t], sel / sel.sum(), rtol=1e-15)
+
+
+def test_group_limited_reduces_to_plain_topk():
+    """One group, or every group kept: the same routing as the plain top-k (itself pinned by
+    brute force above)."""
+    rng = np.random.default_rng(5)
+    key = np.round(rng.standard_normal((300, 16)) * 2) / 2
+    score = rng.uniform(0.1, 1.0, (300, 16))
+    pidx, pw, pm = oracle.topk(key, score, 4)
+    for G, M in ((1, 1), (4, 4), (16, 16)):
+        idx, w, m = oracle.topk_grouped(key, score, 4, G, M)
+        np.testing.assert_array_equal(idx, pidx)
+        np.testing.assert_array_equal(w, pw)
+
+
+def test_group_limited_rejects_bad_shapes():
+    key = np.zeros((1, 8))
+    for G, M, k in ((3, 1, 1), (4, 0, 1), (4, 5, 1), (4, 1, 3)):
+        with pytest.raises(ValueError):
+            oracle.topk_grouped(key, key, k, G, M)
+
+
 # ------------------------------------------------------------------ dispatch tables
 def _random_routing(T, E, k, seed):
     rng = np.random.default_rng(seed)
