@@ -118,9 +118,20 @@ int moe_layer_forward(const moe_shape* s, const void* x, const void* w_router,
 
 typedef struct {
   cudaEvent_t* stage_events; /* NULL, or MOE_NUM_STAGE_EVENTS events created by the caller */
+  /* Group-limited (node-limited) routing, page "Expert-Parallel MoE Inference: Serving Sparse
+   * Models at Scale", section "Load imbalance and how to fight it": node-limited routing caps
+   * how many nodes a token's experts may span.  The experts form n_groups contiguous groups of
+   * E / n_groups (an expert-parallel placement); a group's score is its largest selection key;
+   * the topk_groups best groups are kept (equal scores: the lower group id) and the top-k runs
+   * over their experts only.  0 / 0: plain top-k.  Otherwise 1 <= n_groups <= 32, E divisible
+   * by n_groups, 1 <= topk_groups <= n_groups and topk_groups * E / n_groups >= k, else
+   * MOE_ERR_INVALID_ARG. */
+  int n_groups;
+  int topk_groups;
 } moe_forward_opts;
 
-/* moe_layer_forward with options (stage timing events); opts may be NULL. */
+/* moe_layer_forward with options (stage timing events, group-limited routing); opts may be
+ * NULL. */
 int moe_layer_forward_ex(const moe_shape* s, const void* x, const void* w_router,
                          const void* w_gate_up, const void* w_down, moe_score_fn score_fn,
                          const float* bias, const moe_shared_expert* shared_expert, void* out,
@@ -139,6 +150,14 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
                         int* topk_idx, float* topk_w, int* expert_counts, int* expert_offsets,
                         int* sorted_token, int* slot_pos, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream);
+
+/* moe_route_from_keys with group-limited routing (n_groups >= 1, topk_groups as in
+ * moe_forward_opts); same outputs, workspace and errors. */
+int moe_route_from_keys_grouped(const moe_shape* s, const float* sel_key,
+                                const float* gate_score, int n_groups, int topk_groups,
+                                int* topk_idx, float* topk_w, int* expert_counts,
+                                int* expert_offsets, int* sorted_token, int* slot_pos,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* moe_route_from_keys for callers that cannot allocate device memory (an allocator they do
  * not own, a pool that is already carved up, a C host with no allocator wired in).  The

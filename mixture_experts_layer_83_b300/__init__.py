@@ -26,7 +26,8 @@ MOE_NUM_STAGE_EVENTS = 8
 STAGE_NAMES = ("router_gemm", "topk", "dispatch", "gather", "gateup_gemm", "down_gemm", "combine")
 
 EXPORTED = ("moe_layer_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
-            "moe_route_from_keys", "moe_route_from_keys_noalloc", "moe_debug_gemm_tiles",
+            "moe_route_from_keys", "moe_route_from_keys_grouped", "moe_route_from_keys_noalloc",
+            "moe_debug_gemm_tiles",
             "moe_layer_num_launches", "moe_workspace_status", "moe_status_string")
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -42,7 +43,8 @@ class MoeSharedExpert(ctypes.Structure):
 
 
 class MoeForwardOpts(ctypes.Structure):
-    _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p))]
+    _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_groups", ctypes.c_int),
+                ("topk_groups", ctypes.c_int)]
 
 
 class MoeError(RuntimeError):
@@ -73,6 +75,9 @@ def lib():
         l.moe_layer_forward_ex.restype = ci
         l.moe_route_from_keys.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         l.moe_route_from_keys.restype = ci
+        l.moe_route_from_keys_grouped.argtypes = [shp, vp, vp, ci, ci, vp, vp, vp, vp, vp, vp, vp,
+                                                  sz, vp]
+        l.moe_route_from_keys_grouped.restype = ci
         l.moe_route_from_keys_noalloc.argtypes = [shp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         l.moe_route_from_keys_noalloc.restype = ci
         l.moe_debug_gemm_tiles.argtypes = [shp, ci, ci, vp, vp, ci, vp]
@@ -130,8 +135,9 @@ def _shared(shared_expert):
 def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, shared_expert,
                       out, expert_counts, workspace, workspace_bytes=None, stream=None,
                       topk_idx_out=None, topk_w_out=None, sorted_token_out=None,
-                      stage_events=None, check=True):
-    """One forward pass; ``shared_expert`` is None or (w_gate_up, w_down).  Returns the status
+                      stage_events=None, n_groups=0, topk_groups=0, check=True):
+    """One forward pass; ``shared_expert`` is None or (w_gate_up, w_down); ``n_groups`` /
+    ``topk_groups`` select group-limited routing (0 / 0: plain top-k).  Returns the status
     (raises MoeError on failure when ``check``)."""
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
@@ -139,14 +145,17 @@ def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, sha
             int(score_fn), _ptr(bias), _shared(shared_expert), _ptr(out), _ptr(expert_counts),
             _ptr(workspace), int(workspace_bytes), _stream(stream), _ptr(topk_idx_out),
             _ptr(topk_w_out), _ptr(sorted_token_out)]
-    if stage_events is None:
+    if stage_events is None and n_groups == 0 and topk_groups == 0:
         rc = lib().moe_layer_forward(*args)
     else:
-        for e in stage_events:
-            if not e.cuda_event:   # torch creates the CUDA event on its first record
-                e.record()
-        arr = (ctypes.c_void_p * MOE_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
-        rc = lib().moe_layer_forward_ex(*args, ctypes.byref(MoeForwardOpts(arr)))
+        arr = None
+        if stage_events is not None:
+            for e in stage_events:
+                if not e.cuda_event:   # torch creates the CUDA event on its first record
+                    e.record()
+            arr = (ctypes.c_void_p * MOE_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
+        opts = MoeForwardOpts(arr, int(n_groups), int(topk_groups))
+        rc = lib().moe_layer_forward_ex(*args, ctypes.byref(opts))
     if check and rc != MOE_OK:
         raise MoeError(rc, "moe_layer_forward")
     return rc
@@ -166,6 +175,23 @@ def moe_route_from_keys(shape, sel_key, gate_score, topk_idx, topk_w, expert_cou
                                    _ptr(workspace), int(workspace_bytes), _stream(stream))
     if check and rc != MOE_OK:
         raise MoeError(rc, "moe_route_from_keys")
+    return rc
+
+
+def moe_route_from_keys_grouped(shape, sel_key, gate_score, n_groups, topk_groups, topk_idx,
+                                topk_w, expert_counts, expert_offsets, sorted_token, slot_pos,
+                                workspace, workspace_bytes=None, stream=None, check=True):
+    """moe_route_from_keys with group-limited routing (see include/moe_layer.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().moe_route_from_keys_grouped(ctypes.byref(shape), _ptr(sel_key), _ptr(gate_score),
+                                           int(n_groups), int(topk_groups), _ptr(topk_idx),
+                                           _ptr(topk_w), _ptr(expert_counts),
+                                           _ptr(expert_offsets), _ptr(sorted_token),
+                                           _ptr(slot_pos), _ptr(workspace), int(workspace_bytes),
+                                           _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoeError(rc, "moe_route_from_keys_grouped")
     return rc
 
 

@@ -82,6 +82,15 @@ int check_shape(const moe_shape* s, bool routing_only) {
   return MOE_OK;
 }
 
+// Group-limited routing: G contiguous groups of E / G experts (G <= 32), M kept per token, with
+// room for k experts in the kept groups.  G = 0: plain top-k.
+int check_groups(const moe_shape& s, int G, int M) {
+  if (G == 0 && M == 0) return MOE_OK;
+  if (G < 1 || G > 32 || s.E % G != 0 || M < 1 || M > G || M * (s.E / G) < s.k)
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
 int device_sm_count() {
   static std::mutex mu;
   static int cache[64] = {0};
@@ -350,6 +359,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                               expert_counts, workspace, workspace_bytes, topk_idx_out, topk_w_out,
                               sorted_token_out);
   if (rc != MOE_OK) return rc;
+  const int n_groups = opts ? opts->n_groups : 0, topk_groups = opts ? opts->topk_groups : 0;
+  rc = check_groups(*s, n_groups, topk_groups);
+  if (rc != MOE_OK) return rc;
   const int sms = device_sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   const moe_shape& S = *s;
@@ -392,6 +404,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                                         S.T, S.d, S.E, logits, stream));
   if (!mark(1)) return MOE_ERR_CUDA;
   MOE_TRY(launch_topk(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, logits, nullptr, bias, S.T, S.E, S.k,
+                      n_groups, topk_groups,
                       tidx, tw, stream));
   if (!mark(2)) return MOE_ERR_CUDA;
   MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp,
@@ -423,6 +436,37 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   MOE_TRY(launch_combine(xs_y, slot, tw, S.T, S.k, S.d, R, S.Fs > 0 ? 1 : 0, bf16 ? 1 : 0, out, stream));
   if (!mark(7)) return MOE_ERR_CUDA;
 #undef MOE_TRY
+  return MOE_OK;
+}
+
+int route_from_keys_impl(const moe_shape* s, const float* sel_key, const float* gate_score, int n_groups,
+                         int topk_groups, int* topk_idx, float* topk_w, int* expert_counts,
+                         int* expert_offsets, int* sorted_token, int* slot_pos, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_shape(s, true);
+  if (rc != MOE_OK) return rc;
+  rc = check_groups(*s, n_groups, topk_groups);
+  if (rc != MOE_OK) return rc;
+  const void* ptrs[] = {sel_key, gate_score, topk_idx, topk_w, expert_counts, expert_offsets,
+                        sorted_token, slot_pos, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  // only the layout's leading tables (they depend on T, E and k alone) are used here
+  moe_shape r = *s;
+  r.d = 64;
+  r.F = 64;
+  r.Fs = 0;
+  r.dtype = MOE_DTYPE_BF16;
+  const Layout L = layout_of(r);
+  if (workspace_bytes < L.ntp + align256((size_t)(s->E + 1) * 4)) return MOE_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  if (launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, n_groups, topk_groups, topk_idx,
+                  topk_w, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
+                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
+                      nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -467,29 +511,20 @@ int moe_route_from_keys(const moe_shape* s, const float* sel_key, const float* g
                         int* topk_idx, float* topk_w, int* expert_counts, int* expert_offsets,
                         int* sorted_token, int* slot_pos, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
-  int rc = check_shape(s, true);
-  if (rc != MOE_OK) return rc;
-  const void* ptrs[] = {sel_key, gate_score, topk_idx, topk_w, expert_counts, expert_offsets,
-                        sorted_token, slot_pos, workspace};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
-  // only the layout's leading tables (they depend on T, E and k alone) are used here
-  moe_shape r = *s;
-  r.d = 64;
-  r.F = 64;
-  r.Fs = 0;
-  r.dtype = MOE_DTYPE_BF16;
-  const Layout L = layout_of(r);
-  if (workspace_bytes < L.ntp + align256((size_t)(s->E + 1) * 4)) return MOE_ERR_WORKSPACE;
-  char* ws = static_cast<char*>(workspace);
-  if (launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, topk_idx, topk_w, stream) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
-                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
-                      nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return route_from_keys_impl(s, sel_key, gate_score, 0, 0, topk_idx, topk_w, expert_counts,
+                              expert_offsets, sorted_token, slot_pos, workspace, workspace_bytes,
+                              stream);
+}
+
+int moe_route_from_keys_grouped(const moe_shape* s, const float* sel_key,
+                                const float* gate_score, int n_groups, int topk_groups,
+                                int* topk_idx, float* topk_w, int* expert_counts,
+                                int* expert_offsets, int* sorted_token, int* slot_pos,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (n_groups < 1) return MOE_ERR_INVALID_ARG;
+  return route_from_keys_impl(s, sel_key, gate_score, n_groups, topk_groups, topk_idx, topk_w,
+                              expert_counts, expert_offsets, sorted_token, slot_pos, workspace,
+                              workspace_bytes, stream);
 }
 
 int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,

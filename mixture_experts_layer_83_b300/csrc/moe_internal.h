@@ -76,8 +76,9 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int T, int d, int E,
                                      float* logits, cudaStream_t s);
 // src: 0 = logits + softmax, 1 = logits + sigmoid, 2 = supplied key (a) and score (b).
+// G > 0: group-limited, M of G contiguous expert groups kept per token (G = 0: plain top-k).
 cudaError_t launch_topk(int src, const float* a, const float* b, const float* bias, int T, int E,
-                        int k, int* topk_idx, float* topk_w, cudaStream_t s);
+                        int k, int G, int M, int* topk_idx, float* topk_w, cudaStream_t s);
 
 // Dispatch (moe_dispatch.cu).
 // ntp / ntp2 (either may be null): per-expert prefixes of tile units (seg_units) for n-tile

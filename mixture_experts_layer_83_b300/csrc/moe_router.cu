@@ -42,11 +42,16 @@ __device__ __forceinline__ bool before(float ka, int ea, float kb, int eb) {
 //   SRC 1: a = logits, key = sigmoid(logit), weights = renormalised sigmoids.
 //   SRC 2: a = supplied keys, b = supplied scores, weights = renormalised scores.
 // The optional bias is added to the key (SRC 0/1) and never to the weights.
+// Group-limited routing (G > 0; page "Expert-Parallel MoE Inference", "Load imbalance and how
+// to fight it": node-limited routing caps how many groups of experts a token may span): the
+// experts form G contiguous groups of E / G; a group's score is its largest key; the M best
+// groups are kept (equal scores: the lower group id) and the experts of the other groups are
+// excluded before the k rounds.
 template <int NV, int SRC>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
                                                    const float* __restrict__ b,
                                                    const float* __restrict__ bias, int T, int E,
-                                                   int k, int* __restrict__ topk_idx,
+                                                   int k, int G, int M, int* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -76,6 +81,42 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
       }
       key[v] = kv;
       val[v] = vv;
+    }
+    if (G > 0) {
+      const int gsz = E / G;
+      float my_g = -INFINITY;  // lane g holds group g's score
+      for (int g = 0; g < G; ++g) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          const int e = lane + 32 * v;
+          if (e < E && e / gsz == g) m = fmaxf(m, key[v]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        if (lane == g) my_g = m;
+      }
+      uint32_t gsel = 0;
+      for (int r = 0; r < M; ++r) {
+        const bool cand = lane < G && !((gsel >> lane) & 1u);
+        float bk = cand ? my_g : -INFINITY;
+        int be = cand ? lane : INT_MAX;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ok = __shfl_xor_sync(kFull, bk, off);
+          const int oe = __shfl_xor_sync(kFull, be, off);
+          if (before(ok, oe, bk, be)) {
+            bk = ok;
+            be = oe;
+          }
+        }
+        gsel |= 1u << be;
+      }
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const int e = lane + 32 * v;
+        if (e < E && !((gsel >> (e / gsz)) & 1u)) taken |= 1u << v;
+      }
     }
     int my_e = 0;
     float my_val = 0.f;
@@ -134,16 +175,16 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
 
 template <int NV>
 cudaError_t launch_topk_nv(int src, const float* a, const float* b, const float* bias, int T,
-                           int E, int k, int* idx, float* w, cudaStream_t s) {
+                           int E, int k, int G, int M, int* idx, float* w, cudaStream_t s) {
   const int threads = 256, wpb = threads / 32;
   int blocks = (T + wpb - 1) / wpb;
   if (blocks > 148 * 32) blocks = 148 * 32;
   if (src == 0)
-    topk_kernel<NV, 0><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, idx, w);
+    topk_kernel<NV, 0><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w);
   else if (src == 1)
-    topk_kernel<NV, 1><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, idx, w);
+    topk_kernel<NV, 1><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w);
   else
-    topk_kernel<NV, 2><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, idx, w);
+    topk_kernel<NV, 2><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w);
   return cudaGetLastError();
 }
 
@@ -159,14 +200,14 @@ cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int 
 }
 
 cudaError_t launch_topk(int src, const float* a, const float* b, const float* bias, int T, int E,
-                        int k, int* topk_idx, float* topk_w, cudaStream_t s) {
+                        int k, int G, int M, int* topk_idx, float* topk_w, cudaStream_t s) {
   const int nv = (E + 31) / 32;
-  if (nv <= 1) return launch_topk_nv<1>(src, a, b, bias, T, E, k, topk_idx, topk_w, s);
-  if (nv <= 2) return launch_topk_nv<2>(src, a, b, bias, T, E, k, topk_idx, topk_w, s);
-  if (nv <= 4) return launch_topk_nv<4>(src, a, b, bias, T, E, k, topk_idx, topk_w, s);
-  if (nv <= 8) return launch_topk_nv<8>(src, a, b, bias, T, E, k, topk_idx, topk_w, s);
-  if (nv <= 16) return launch_topk_nv<16>(src, a, b, bias, T, E, k, topk_idx, topk_w, s);
-  return launch_topk_nv<32>(src, a, b, bias, T, E, k, topk_idx, topk_w, s);
+  if (nv <= 1) return launch_topk_nv<1>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
+  if (nv <= 2) return launch_topk_nv<2>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
+  if (nv <= 4) return launch_topk_nv<4>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
+  if (nv <= 8) return launch_topk_nv<8>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
+  if (nv <= 16) return launch_topk_nv<16>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
+  return launch_topk_nv<32>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
 }
 
 }  // namespace moe

@@ -5,6 +5,9 @@ same inputs, and compare them the way the layer's correctness criteria read:
   keys) is at least ``MARGIN``; a token under the margin may pick either side of the near-tie,
   but its choice must be a valid top-k of the oracle keys up to ``MARGIN``;
 * dispatch tables: bit-exact against the oracle's tables for the GPU's routing;
+* group-limited routing (a workload with ``topk_groups`` > 0 keeps that many of its ``groups``
+  expert groups per token): the same, against the oracle's group-limited top-k, whose margin
+  also covers near-ties between groups;
 * output: max |err| <= 2e-2 * max |ref| and sum |err| / sum |ref| <= 5e-3 for bf16 (tighter
   for fp32), the oracle evaluated under the GPU's routing, so an accepted near-tie does not
   count as an output error.
@@ -44,7 +47,7 @@ def gpu_forward(cfg, dev, stream=None, workspace=None, stage_events=None):
     shared = (dev["sh_gate_up"], dev["sh_down"]) if c["Fs"] > 0 else None
     moe.moe_layer_forward(shape, dev["x"], dev["w_router"], dev["w_gate_up"], dev["w_down"],
                           c["score"], dev.get("bias"), shared, out, counts, workspace, ws_bytes,
-                          stream, tidx, tw, st, stage_events=stage_events)
+                          stream, tidx, tw, st, stage_events=stage_events, **group_args(c))
     return dict(out=out, counts=counts, topk_idx=tidx, topk_w=tw, sorted_token=st,
                 workspace=workspace)
 
@@ -62,13 +65,25 @@ def to_host(res):
     return h
 
 
+def group_args(cfg):
+    """Group-limited routing options of a workload (none unless it sets topk_groups)."""
+    c = configs.get(cfg)
+    if c.get("topk_groups", 0) > 0:
+        return dict(n_groups=c["groups"], topk_groups=c["topk_groups"])
+    return {}
+
+
 def oracle_routing(cfg, x, w_router, bias, threads=None):
     """fp64 oracle logits -> (key, score, topk_idx, margin) for all rows of x (host arrays)."""
     c = configs.get(cfg)
+    g = group_args(c)
 
     def part(lo, hi):
         lg, sc, key = oracle.router_scores(x[lo:hi], w_router, c["score"], bias)
-        idx, _, margin = oracle.topk(key, sc, c["k"])
+        if g:
+            idx, _, margin = oracle.topk_grouped(key, sc, c["k"], g["n_groups"], g["topk_groups"])
+        else:
+            idx, _, margin = oracle.topk(key, sc, c["k"])
         return key, sc, idx, margin
 
     parts = oracle.parallel_rows(part, x.shape[0], threads=threads)
@@ -91,9 +106,15 @@ def check_routing(cfg, key, score, margin, o_idx, g_idx, g_w):
         f"t={bad[0]} gpu={g_idx[bad[0]]} oracle={o_idx[bad[0]]} margin={margin[bad[0]]}"
     rows = np.arange(T)[:, None]
     sel_key = key[rows, g_idx]
-    masked = key.copy()
-    masked[rows, g_idx] = -np.inf
-    if k < c["E"]:
+    g = group_args(c)
+    if g:
+        # a group-limited choice spans at most topk_groups groups
+        gs = c["E"] // g["n_groups"]
+        spans = np.array([len(set((g_idx[t] // gs).tolist())) for t in range(T)])
+        assert np.all(spans <= g["topk_groups"]), "routing spans too many groups"
+    elif k < c["E"]:
+        masked = key.copy()
+        masked[rows, g_idx] = -np.inf
         gap = sel_key.min(1) - masked.max(1)
         assert np.all(gap >= -MARGIN), f"invalid near-tie choice, gap {gap.min()}"
     # GPU order: non-increasing oracle key up to the margin

@@ -234,3 +234,18 @@ def test_gateup_tall_and_wide_tiles():
         else:          # wide: two consecutive weight tiles (a pair)
             assert (t[:, 2].reshape(-1, 2) == t[::2, 2:3] + np.arange(2)).all()
     assert (routed[:, 1] != 2).all()
+
+
+def test_group_limited_routing_arguments_are_checked_before_launch():
+    """Invalid group options are rejected on the host (fake pointers never reach a kernel)."""
+    s = shape(T=16, E=64, k=8)
+    args = [16] * 8
+    for G, M in ((3, 1), (0, 1), (64, 1), (8, 0), (8, 9), (8, 1), (33, 2)):
+        # (8, 1): 1 group of 8 experts holds exactly k = 8 -> allowed; every other case invalid
+        rc = moe.moe_route_from_keys_grouped(s, 16, 16, G, M, *args[:6], 16, 1 << 30, stream=0,
+                                             check=False) if (G, M) != (8, 1) else None
+        if rc is not None:
+            assert rc == moe.MOE_ERR_INVALID_ARG, (G, M, rc)
+    s2 = shape(T=16, E=64, k=9)
+    assert moe.moe_route_from_keys_grouped(s2, 16, 16, 8, 1, *args[:6], 16, 1 << 30, stream=0,
+                                           check=False) == moe.MOE_ERR_INVALID_ARG

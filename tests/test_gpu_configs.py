@@ -29,3 +29,16 @@ def test_full_size_config(cfg_id):
     print(c["name"], stats)
     del dev
     torch.cuda.empty_cache()
+
+
+def test_full_size_skewed_layer_with_group_limited_routing():
+    """The Zipf-skewed layer (128 experts in its 8 contiguous groups of 16) with each token's
+    experts limited to its 4 best groups: routing, dispatch tables and sampled outputs against
+    the oracle's group-limited top-k."""
+    c = dict(configs.CONFIGS[4], topk_groups=4)
+    dev = moe_inputs.device_inputs(c)
+    torch.cuda.synchronize()
+    stats = sampled_check(c, dev, n_sample=SAMPLE[4])
+    print(c["name"], "group-limited", stats)
+    del dev
+    torch.cuda.empty_cache()

@@ -129,6 +129,57 @@ def test_route_from_keys_is_bit_exact(T, E, k, score, ties):
     np.testing.assert_allclose(w.cpu().numpy(), o_w, rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("T,E,k,G,M,score,ties", [(1000, 256, 8, 8, 4, SIGMOID, False),
+                                                  (2500, 128, 8, 8, 4, SOFTMAX, True),
+                                                  (700, 64, 6, 4, 2, SOFTMAX, True),
+                                                  (300, 40, 5, 5, 2, SIGMOID, True),
+                                                  (100, 32, 4, 32, 4, SOFTMAX, True),
+                                                  (50, 24, 3, 8, 1, SIGMOID, True)])
+def test_route_from_keys_grouped_is_bit_exact(T, E, k, G, M, score, ties):
+    """Group-limited routing on oracle-supplied fp32 keys: top-k sets and order, counts,
+    offsets, permutation and slot positions equal to the oracle's group-limited top-k."""
+    import mixture_experts_layer_83_b300 as moe
+    key, sc = _oracle_keys(T, E, score, seed=T + E + k + G, ties=ties)
+    o_idx, o_w, _ = oracle.topk_grouped(key.astype(np.float64), sc.astype(np.float64), k, G, M)
+    o_counts, o_off, o_st, o_sp = oracle.dispatch(o_idx, E)
+    dev = "cuda"
+    kk, ss = torch.from_numpy(key).to(dev), torch.from_numpy(sc).to(dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    st = torch.empty(T * k, dtype=torch.int32, device=dev)
+    sp = torch.empty((T, k), dtype=torch.int32, device=dev)
+    shape = moe.make_shape(T, 64, E, k, 64)
+    ws = torch.empty(moe.moe_layer_workspace_size(shape), dtype=torch.uint8, device=dev)
+    moe.moe_route_from_keys_grouped(shape, kk, ss, G, M, idx, w, counts, off, st, sp, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), o_idx)
+    np.testing.assert_array_equal(counts.cpu().numpy(), o_counts)
+    np.testing.assert_array_equal(off.cpu().numpy(), o_off)
+    np.testing.assert_array_equal(st.cpu().numpy(), o_st)
+    np.testing.assert_array_equal(sp.cpu().numpy(), o_sp)
+    np.testing.assert_allclose(w.cpu().numpy(), o_w, rtol=2e-6, atol=1e-7)
+
+
+GROUPED = {
+    # 64 experts in 8 groups, 3 kept: sigmoid + bias with a shared expert
+    "bf16_sigmoid_groups": dict(make_shape(500, 256, 64, 8, 128, Fs=64, score=SIGMOID,
+                                           bias_range=0.01, seed=31), groups=8, topk_groups=3),
+    # softmax, 4 groups of 8, 2 kept
+    "bf16_softmax_groups": dict(make_shape(400, 192, 32, 4, 192, seed=32), groups=4,
+                                topk_groups=2),
+    # one group kept: every token's experts come from a single group of 8
+    "bf16_one_group": dict(make_shape(300, 128, 64, 4, 64, seed=33), groups=8, topk_groups=1),
+}
+
+
+@pytest.mark.parametrize("name", list(GROUPED))
+def test_group_limited_layer_matches_oracle(name):
+    stats = full_check(GROUPED[name])
+    print(name, stats)
+
+
 def test_forward_dispatch_tables_match_oracle_for_gpu_routing():
     cfg = SMALL["bf16_many_experts"]
     dev = moe_inputs.upload(cfg, moe_inputs.host_inputs(cfg))
