@@ -56,11 +56,14 @@ def lib():
         l.oracle_topk.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_topk_grouped.argtypes = [ci, ci, ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_dispatch.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
+        l.oracle_capacity.argtypes = [ci, ci, ci, ctypes.c_double]
+        l.oracle_dispatch_capacity.argtypes = [ci, ci, ci, vp, ci, vp, vp, vp, vp, vp]
         l.oracle_gather.argtypes = [ci, ci, vp, vp, vp]
         l.oracle_combine.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_swiglu_ffn.argtypes = [ci, ci, ci, vp, vp, vp, vp]
         l.oracle_layer_rows.argtypes = [ctypes.POINTER(OracleLayer), ci, vp, vp, vp, vp]
         for f in ("oracle_router_scores", "oracle_topk", "oracle_topk_grouped", "oracle_dispatch",
+                  "oracle_capacity", "oracle_dispatch_capacity",
                   "oracle_gather",
                   "oracle_combine", "oracle_swiglu_ffn", "oracle_layer_rows"):
             getattr(l, f).restype = ci
@@ -127,6 +130,27 @@ def dispatch(topk_idx, E):
     _check(lib().oracle_dispatch(T, E, k, _p(topk_idx), _p(counts), _p(offsets), _p(st), _p(sp)),
            "dispatch")
     return counts, offsets, st, sp
+
+
+def capacity(T, E, k, capacity_factor):
+    c = lib().oracle_capacity(T, E, k, float(capacity_factor))
+    if c < 0:
+        raise ValueError("capacity: bad arguments")
+    return c
+
+
+def dispatch_capacity(topk_idx, E, cap):
+    """Dispatch with an expert capacity (see moe_oracle.h):
+    (counts, offsets, sorted_token, slot_pos with -1 for dropped, dropped)."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = topk_idx.shape
+    counts = np.empty(E, dtype=np.int32); offsets = np.empty(E + 1, dtype=np.int32)
+    st = np.empty(T * k, dtype=np.int32); sp = np.empty((T, k), dtype=np.int32)
+    dropped = np.zeros(1, dtype=np.int32)
+    _check(lib().oracle_dispatch_capacity(T, E, k, _p(topk_idx), int(cap), _p(counts),
+                                          _p(offsets), _p(st), _p(sp), _p(dropped)),
+           "dispatch_capacity")
+    return counts, offsets, st[:offsets[-1]], sp, int(dropped[0])
 
 
 def gather(sorted_token, x):

@@ -210,6 +210,50 @@ int oracle_dispatch(int T, int E, int k, const int* topk_idx, int* counts, int* 
   return 0;
 }
 
+/* Expert capacity (page "Expert-Parallel MoE Inference: Serving Sparse Models at Scale",
+ * section "Capacity factor and token dropping"): capacity = capacity_factor * (tokens * k /
+ * experts) slots per expert, rounded up to a whole slot (the pages do not say how a fractional
+ * capacity is rounded; up keeps at least the average load).  Each routed token checks whether
+ * its expert still has a free slot: tokens claim slots in token order, the first `capacity`
+ * assignments of an expert are dispatched and the rest are dropped (they skip the FFN).
+ * counts[e] = dispatched assignments of e, offsets its exclusive prefix sum, sorted_token the
+ * dispatched tokens expert by expert in token order, slot_pos[t][j] their positions or -1 when
+ * dropped; *dropped = number of dropped assignments. */
+int oracle_capacity(int T, int E, int k, double capacity_factor) {
+  if (T < 0 || E < 1 || k < 1 || !(capacity_factor > 0.0)) return -1;
+  return (int)ceil(capacity_factor * ((double)T * (double)k / (double)E));
+}
+
+int oracle_dispatch_capacity(int T, int E, int k, const int* topk_idx, int capacity,
+                             int* counts, int* offsets, int* sorted_token, int* slot_pos,
+                             int* dropped) {
+  if (T < 0 || E < 1 || k < 1 || capacity < 0 || !topk_idx || !counts || !offsets) return -1;
+  for (size_t i = 0; i < (size_t)T * k; ++i)
+    if (topk_idx[i] < 0 || topk_idx[i] >= E) return -1;
+  int ndrop = 0, p = 0;
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    int claimed = 0;
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j)
+        if (topk_idx[(size_t)t * k + j] == e) {
+          if (claimed < capacity) {
+            if (sorted_token) sorted_token[p] = t;
+            if (slot_pos) slot_pos[(size_t)t * k + j] = p;
+            ++p;
+            ++claimed;
+          } else {
+            if (slot_pos) slot_pos[(size_t)t * k + j] = -1;
+            ++ndrop;
+          }
+        }
+    counts[e] = claimed;
+    offsets[e + 1] = offsets[e] + claimed;
+  }
+  if (dropped) *dropped = ndrop;
+  return 0;
+}
+
 int oracle_gather(int R, int d, const int* sorted_token, const double* x, double* xs) {
   if (R < 0 || d < 1 || !sorted_token || !x || !xs) return -1;
   for (int p = 0; p < R; ++p)
@@ -226,8 +270,11 @@ int oracle_combine(int T, int k, int d, const int* slot_pos, const double* topk_
   for (int t = 0; t < T; ++t)
     for (int c = 0; c < d; ++c) {
       double acc = 0.0;
-      for (int j = 0; j < k; ++j)
-        acc += topk_w[(size_t)t * k + j] * ys[(size_t)slot_pos[(size_t)t * k + j] * d + c];
+      for (int j = 0; j < k; ++j) {
+        const int p = slot_pos[(size_t)t * k + j];
+        if (p < 0) continue;  /* an assignment dropped at capacity contributes nothing */
+        acc += topk_w[(size_t)t * k + j] * ys[(size_t)p * d + c];
+      }
       if (y_shared) acc += y_shared[(size_t)t * d + c];
       out[(size_t)t * d + c] = acc;
     }

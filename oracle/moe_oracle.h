@@ -74,10 +74,22 @@ int oracle_topk_grouped(int n_tok, int E, int k, int n_groups, int topk_groups,
 int oracle_dispatch(int T, int E, int k, const int* topk_idx, int* counts, int* offsets,
                     int* sorted_token, int* slot_pos);
 
+/* Expert capacity: ceil(capacity_factor * T * k / E) (capacity_factor > 0), or -1. */
+int oracle_capacity(int T, int E, int k, double capacity_factor);
+
+/* Dispatch with an expert capacity: per expert, the first `capacity` assignments in token
+ * order are dispatched and the rest dropped.  counts [E] = dispatched per expert, offsets
+ * [E+1], sorted_token [dispatched total], slot_pos [T][k] = position or -1 (dropped),
+ * *dropped = dropped assignments (any output except counts / offsets may be NULL). */
+int oracle_dispatch_capacity(int T, int E, int k, const int* topk_idx, int capacity,
+                             int* counts, int* offsets, int* sorted_token, int* slot_pos,
+                             int* dropped);
+
 /* xs[p] = x[sorted_token[p]] for p < R (fp64 rows of width d). */
 int oracle_gather(int R, int d, const int* sorted_token, const double* x, double* xs);
 
-/* out[t] = sum_j topk_w[t][j] * ys[slot_pos[t][j]] (+ y_shared[t] if not NULL). */
+/* out[t] = sum_j topk_w[t][j] * ys[slot_pos[t][j]] (+ y_shared[t] if not NULL); a slot_pos
+ * of -1 (an assignment dropped at capacity) contributes nothing. */
 int oracle_combine(int T, int k, int d, const int* slot_pos, const double* topk_w,
                    const double* ys, const double* y_shared, double* out);
 

@@ -266,6 +266,81 @@ def test_dispatch_reproduces_capacity_worked_example():
     assert round(skew * per_gpu.mean()) == g["expected"]["busiest_gpu_token_experts_approx"]
 
 
+# ------------------------------------------------------------------ expert capacity
+def test_capacity_formula_on_the_worked_example():
+    """Page formula capacity = capacity_factor * (tokens * k / experts): the worked example's
+    512 decode tokens, top-8 of 256 experts give 16 slots at factor 1.0, 20 at 1.25 and 32 at
+    2.0; a fractional capacity rounds up (200 / 7 = 28.57 -> 29)."""
+    g = json.load(open(os.path.join(GOLDEN, "capacity_worked_example.json")))
+    T, E, k = g["tokens"], g["n_experts"], g["top_k"]
+    assert oracle.capacity(T, E, k, 1.0) == g["expected"]["tokens_per_expert_uniform"] == 16
+    assert oracle.capacity(T, E, k, 1.25) == 20 and oracle.capacity(T, E, k, 2.0) == 32
+    assert oracle.capacity(100, 7, 2, 1.0) == 29
+    with pytest.raises(ValueError):
+        oracle.capacity(10, 4, 2, 0.0)
+
+
+def test_capacity_hand_case():
+    """5 tokens, 2 experts, top-1, routed [0,0,0,1,0], capacity 2: expert 0 keeps tokens 0 and
+    1, tokens 2 and 4 are dropped (slot -1), expert 1 keeps token 3."""
+    counts, offsets, st, sp, dropped = oracle.dispatch_capacity(
+        np.array([[0], [0], [0], [1], [0]]), 2, 2)
+    assert counts.tolist() == [2, 1] and offsets.tolist() == [0, 2, 3]
+    assert st.tolist() == [0, 1, 3] and sp[:, 0].tolist() == [0, 1, -1, 2, -1]
+    assert dropped == 2
+
+
+@pytest.mark.parametrize("T,E,k,cap", [(40, 6, 2, 5), (100, 16, 5, 20), (64, 8, 8, 64),
+                                       (33, 4, 3, 1), (10, 3, 2, 0)])
+def test_capacity_dispatch_invariants(T, E, k, cap):
+    """Skewed random routings: kept per expert = min(routed, capacity); the kept assignments
+    of an expert are its `capacity` lowest token ids; kept + dropped = T*k; kept slots are a
+    bijection onto [0, kept total) consistent with sorted_token.  Catches: dropping by arrival
+    slot j instead of token order, counts before capping, off-by-one at the capacity."""
+    rng = np.random.default_rng(T * 7 + E + k + cap)
+    p = rng.dirichlet(np.full(E, 0.3))
+    idx = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    counts, offsets, st, sp, dropped = oracle.dispatch_capacity(idx, E, cap)
+    routed = np.bincount(idx.ravel(), minlength=E)
+    np.testing.assert_array_equal(counts, np.minimum(routed, cap))
+    assert counts.sum() + dropped == T * k
+    for e in range(E):
+        toks = sorted(t for t in range(T) if e in idx[t])
+        kept = sorted(int(t) for t, j in zip(*np.where(idx == e)) if sp[t, j] >= 0)
+        assert kept == toks[:cap]
+        seg = st[offsets[e]:offsets[e + 1]].tolist()
+        assert seg == kept
+    kept_slots = sp[sp >= 0]
+    assert sorted(kept_slots.tolist()) == list(range(counts.sum()))
+    for t, j in zip(*np.where(sp >= 0)):
+        assert st[sp[t, j]] == t
+
+
+def test_capacity_large_enough_is_dropless():
+    """A capacity of T (no expert can hold more) reproduces the dropless dispatch."""
+    idx = _random_routing(80, 10, 3, 4)
+    a = oracle.dispatch(idx, 10)
+    b = oracle.dispatch_capacity(idx, 10, 80)
+    for x, y in zip(a, b[:4]):
+        np.testing.assert_array_equal(x, y)
+    assert b[4] == 0
+
+
+def test_combine_skips_dropped_assignments():
+    """Identity experts with some assignments dropped: out[t] = (sum of the kept weights) x[t]."""
+    rng = np.random.default_rng(9)
+    T, E, k, d = 30, 5, 2, 4
+    x = rng.standard_normal((T, d))
+    idx = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.dirichlet(np.ones(k), T)
+    counts, offsets, st, sp, dropped = oracle.dispatch_capacity(idx, E, 7)
+    assert dropped > 0
+    ys = oracle.gather(st, x)
+    out = oracle.combine(sp, w, ys)
+    kept_w = np.where(sp >= 0, w, 0.0).sum(1)
+    np.testing.assert_allclose(out, kept_w[:, None] * x, rtol=1e-14, atol=1e-14)
+
+
 def test_identity_experts_round_trip_returns_x():
     """Dispatch (gather) then combine with identity experts returns x (weights sum to 1)."""
     rng = np.random.default_rng(5)
