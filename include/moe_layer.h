@@ -128,6 +128,14 @@ typedef struct {
    * MOE_ERR_INVALID_ARG. */
   int n_groups;
   int topk_groups;
+  /* Expert capacity (same page, section "Capacity factor and token dropping"): each expert
+   * takes at most capacity = ceil(capacity_factor * T * k / E) assignments; tokens claim an
+   * expert's slots in token order and an assignment beyond the capacity is dropped: it skips
+   * the expert FFN and contributes nothing to its token's output (the token's other weights
+   * are not renormalised; the layer output carries no residual).  expert_counts then counts
+   * the dispatched assignments.  0: dropless.  Negative, NaN or infinite: MOE_ERR_INVALID_ARG. */
+  float capacity_factor;
+  int* dropped; /* NULL, or a device int (16-byte aligned) receiving the dropped assignments */
 } moe_forward_opts;
 
 /* moe_layer_forward with options (stage timing events, group-limited routing); opts may be

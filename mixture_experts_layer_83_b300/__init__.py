@@ -44,7 +44,8 @@ class MoeSharedExpert(ctypes.Structure):
 
 class MoeForwardOpts(ctypes.Structure):
     _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_groups", ctypes.c_int),
-                ("topk_groups", ctypes.c_int)]
+                ("topk_groups", ctypes.c_int), ("capacity_factor", ctypes.c_float),
+                ("dropped", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -135,17 +136,20 @@ def _shared(shared_expert):
 def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, shared_expert,
                       out, expert_counts, workspace, workspace_bytes=None, stream=None,
                       topk_idx_out=None, topk_w_out=None, sorted_token_out=None,
-                      stage_events=None, n_groups=0, topk_groups=0, check=True):
+                      stage_events=None, n_groups=0, topk_groups=0, capacity_factor=0.0,
+                      dropped=None, check=True):
     """One forward pass; ``shared_expert`` is None or (w_gate_up, w_down); ``n_groups`` /
-    ``topk_groups`` select group-limited routing (0 / 0: plain top-k).  Returns the status
-    (raises MoeError on failure when ``check``)."""
+    ``topk_groups`` select group-limited routing (0 / 0: plain top-k); ``capacity_factor`` > 0
+    caps each expert's assignments (``dropped``: optional device int receiving the number
+    dropped).  Returns the status (raises MoeError on failure when ``check``)."""
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     args = [ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
             int(score_fn), _ptr(bias), _shared(shared_expert), _ptr(out), _ptr(expert_counts),
             _ptr(workspace), int(workspace_bytes), _stream(stream), _ptr(topk_idx_out),
             _ptr(topk_w_out), _ptr(sorted_token_out)]
-    if stage_events is None and n_groups == 0 and topk_groups == 0:
+    if stage_events is None and n_groups == 0 and topk_groups == 0 and capacity_factor == 0 \
+            and dropped is None:
         rc = lib().moe_layer_forward(*args)
     else:
         arr = None
@@ -154,7 +158,8 @@ def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, sha
                 if not e.cuda_event:   # torch creates the CUDA event on its first record
                     e.record()
             arr = (ctypes.c_void_p * MOE_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
-        opts = MoeForwardOpts(arr, int(n_groups), int(topk_groups))
+        opts = MoeForwardOpts(arr, int(n_groups), int(topk_groups), float(capacity_factor),
+                              _ptr(dropped))
         rc = lib().moe_layer_forward_ex(*args, ctypes.byref(opts))
     if check and rc != MOE_OK:
         raise MoeError(rc, "moe_layer_forward")

@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <limits.h>
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -89,6 +90,15 @@ int check_groups(const moe_shape& s, int G, int M) {
   if (G < 1 || G > 32 || s.E % G != 0 || M < 1 || M > G || M * (s.E / G) < s.k)
     return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+// Expert capacity for a capacity factor: ceil(factor * T * k / E) dispatched assignments per
+// expert, INT_MAX for a factor of 0 (dropless).  -1: an invalid factor.
+int capacity_of(const moe_shape& s, float factor) {
+  if (factor == 0.f) return INT_MAX;
+  if (!(factor > 0.f) || !isfinite(factor)) return -1;
+  const double c = ceil((double)factor * ((double)s.T * (double)s.k / (double)s.E));
+  return c >= (double)INT_MAX ? INT_MAX : (int)c;
 }
 
 int device_sm_count() {
@@ -362,6 +372,10 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   const int n_groups = opts ? opts->n_groups : 0, topk_groups = opts ? opts->topk_groups : 0;
   rc = check_groups(*s, n_groups, topk_groups);
   if (rc != MOE_OK) return rc;
+  const int capacity = capacity_of(*s, opts ? opts->capacity_factor : 0.f);
+  if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  int* dropped = opts ? opts->dropped : nullptr;
+  if (dropped != nullptr && !aligned16(dropped)) return MOE_ERR_INVALID_ARG;
   const int sms = device_sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   const moe_shape& S = *s;
@@ -409,9 +423,10 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   if (!mark(2)) return MOE_ERR_CUDA;
   MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp,
                           bf16 ? gateup_bn(S) : 0, bf16 ? gateup_tall_rows(S) : 0,
-                          bf16 ? ntp2 : nullptr, sorted, slot, stream));
+                          bf16 ? ntp2 : nullptr, capacity, dropped, sorted, slot, stream));
   if (!mark(3)) return MOE_ERR_CUDA;
-  MOE_TRY(launch_gather(x, sorted, R, S.d, bf16 ? 2 : 4, xs_y, stream));
+  MOE_TRY(launch_gather(x, sorted, R, capacity == INT_MAX ? nullptr : offsets + S.E, S.d,
+                        bf16 ? 2 : 4, xs_y, stream));
   if (!mark(4)) return MOE_ERR_CUDA;
   if (bf16) {
     MOE_TRY(launch_gemm_tc(kModeGateUp, pl.gateup, sms, stream));
@@ -465,7 +480,7 @@ int route_from_keys_impl(const moe_shape* s, const float* sel_key, const float* 
     return MOE_ERR_CUDA;
   if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
                       expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
-                      nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
+                      nullptr, INT_MAX, nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

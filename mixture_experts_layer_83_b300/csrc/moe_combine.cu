@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(
     for (int v = lane; v < nvec; v += 32) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < k; ++j)
-        acc_bf16x8(acc, __ldg(y + (size_t)s_pos[warp][j] * nvec + v), s_w[warp][j]);
+        if (s_pos[warp][j] >= 0)  // an assignment dropped at capacity contributes nothing
+          acc_bf16x8(acc, __ldg(y + (size_t)s_pos[warp][j] * nvec + v), s_w[warp][j]);
       if (has_shared) acc_bf16x8(acc, __ldg(y + (size_t)(R + t) * nvec + v), 1.f);
       uint4 o;
       __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(256) combine_f32_kernel(
       for (int j = 0; j < k; ++j) {
         const int p = __shfl_sync(kFull, my_pos, j);
         const float wj = __shfl_sync(kFull, my_w, j);
-        if (c < d) acc = fmaf(wj, y[(size_t)p * d + c], acc);
+        if (c < d && p >= 0) acc = fmaf(wj, y[(size_t)p * d + c], acc);
       }
       if (c < d) {
         if (has_shared) acc += y[(size_t)(R + t) * d + c];

@@ -11,6 +11,10 @@
 //      over the warps, then position = offsets[e] + chunk base + warp base + rank among the
 //      earlier equal lanes.  Assignment i = t*k + j, so the order is token order.
 //   4. gather: xs[p] = x[sorted_token[p]], one warp per row, 16-byte vectors.
+// With an expert capacity (page "Expert-Parallel MoE Inference", section "Capacity factor and
+// token dropping"), an assignment whose rank among its expert's assignments (token order) is
+// capacity or more is dropped: slot_pos = -1, no row in the permutation; expert_counts,
+// offsets and the tile prefixes count the dispatched assignments only.
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
@@ -66,7 +70,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ c
                                                              int* __restrict__ expert_counts,
                                                              int* __restrict__ offsets,
                                                              int* __restrict__ ntp, int bn2,
-                                                             int tall2, int* __restrict__ ntp2) {
+                                                             int tall2, int* __restrict__ ntp2,
+                                                             int capacity, int* __restrict__ dropped) {
   __shared__ int scratch[32];
   const int e = threadIdx.x;
   int tot = 0;
@@ -78,11 +83,15 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ c
       tot += v;
     }
   }
+  const int routed = tot;
+  tot = tot < capacity ? tot : capacity;  // dispatched assignments
   const int nt = seg_units(tot, bn, 0);
   const int nt2 = bn2 > 0 ? seg_units(tot, bn2, tall2) : 0;
   const int inc_rows = block_inclusive_scan(tot, scratch);
   const int inc_nt = block_inclusive_scan(nt, scratch);
   const int inc_nt2 = block_inclusive_scan(nt2, scratch);
+  const int inc_drop = block_inclusive_scan(routed - tot, scratch);
+  if (dropped != nullptr && e == 1023) *dropped = inc_drop;
   if (e < E) {
     expert_counts[e] = tot;
     offsets[e] = inc_rows - tot;
@@ -98,7 +107,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ c
 
 __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
     const int* __restrict__ topk_idx, int R, int E, int k, const int* __restrict__ chunk_base,
-    const int* __restrict__ offsets, int* __restrict__ sorted_token, int* __restrict__ slot_pos) {
+    const int* __restrict__ offsets, int capacity, int* __restrict__ sorted_token,
+    int* __restrict__ slot_pos) {
   extern __shared__ int wcount[];  // [kDispatchWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) wcount[i] = 0;
@@ -114,8 +124,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
     __syncwarp();
   }
   __syncthreads();
+  // per expert and warp: the rank (token order) of the warp's first assignment of the expert
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = offsets[e] + chunk_base[(size_t)blockIdx.x * E + e];
+    int run = chunk_base[(size_t)blockIdx.x * E + e];
     for (int w = 0; w < kDispatchWarps; ++w) {
       const int c = wcount[w * E + e];
       wcount[w * E + e] = run;
@@ -128,11 +139,15 @@ __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
     const int i = base + r + lane;
     const int e = i < R ? topk_idx[i] : -1 - lane;
     const unsigned peers = __match_any_sync(kFull, e);
-    int pos = 0;
     if (i < R) {
-      pos = mine[e] + __popc(peers & lt);
-      slot_pos[i] = pos;
-      sorted_token[pos] = i / k;
+      const int rank = mine[e] + __popc(peers & lt);
+      if (rank < capacity) {
+        const int pos = offsets[e] + rank;
+        slot_pos[i] = pos;
+        sorted_token[pos] = i / k;
+      } else {
+        slot_pos[i] = -1;  // dropped at the expert's capacity
+      }
     }
     __syncwarp();
     if (i < R && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
@@ -140,9 +155,12 @@ __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
   }
 }
 
-// One warp per destination row; 16-byte vectors, four loads in flight per lane per step.
+// One warp per destination row; 16-byte vectors, four loads in flight per lane per step.  The
+// row count is *rows_dev when given (rows dispatched under a capacity), else R.
 __global__ void gather_rows_v16_kernel(const uint4* __restrict__ x, const int* __restrict__ sorted_token,
-                                       int R, int row_vecs, uint4* __restrict__ xs) {
+                                       int R, const int* __restrict__ rows_dev, int row_vecs,
+                                       uint4* __restrict__ xs) {
+  if (rows_dev != nullptr) R = *rows_dev;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -163,7 +181,9 @@ __global__ void gather_rows_v16_kernel(const uint4* __restrict__ x, const int* _
 }
 
 __global__ void gather_rows_w4_kernel(const uint32_t* __restrict__ x, const int* __restrict__ sorted_token,
-                                      int R, int row_words, uint32_t* __restrict__ xs) {
+                                      int R, const int* __restrict__ rows_dev, int row_words,
+                                      uint32_t* __restrict__ xs) {
+  if (rows_dev != nullptr) R = *rows_dev;
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -178,33 +198,36 @@ __global__ void gather_rows_w4_kernel(const uint32_t* __restrict__ x, const int*
 
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
                             int* expert_counts, int* offsets, int* ntp, int bn2, int tall2,
-                            int* ntp2, int* sorted_token, int* slot_pos, cudaStream_t s) {
+                            int* ntp2, int capacity, int* dropped, int* sorted_token,
+                            int* slot_pos, cudaStream_t s) {
   const int R = T * k;
   const int nchunks = (R + kDispatchChunk - 1) / kDispatchChunk;
   dispatch_count_kernel<<<nchunks, 256, E * sizeof(int), s>>>(topk_idx, R, E, chunk_counts);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, bn, expert_counts, offsets, ntp,
-                                          bn2, tall2, ntp2);
+                                          bn2, tall2, ntp2, capacity, dropped);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dispatch_scatter_kernel<<<nchunks, kDispatchWarps * 32, kDispatchWarps * E * sizeof(int), s>>>(
-      topk_idx, R, E, k, chunk_counts, offsets, sorted_token, slot_pos);
+      topk_idx, R, E, k, chunk_counts, offsets, capacity, sorted_token, slot_pos);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const void* x, const int* sorted_token, int R, int d, int elt_bytes,
-                          void* xs, cudaStream_t s) {
+cudaError_t launch_gather(const void* x, const int* sorted_token, int R, const int* rows_dev,
+                          int d, int elt_bytes, void* xs, cudaStream_t s) {
   const size_t row_bytes = (size_t)d * elt_bytes;
   const int threads = 256;
   int blocks = (R + 7) / 8;
   if (blocks > 148 * 16) blocks = 148 * 16;
   if (row_bytes % 16 == 0)
     gather_rows_v16_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), sorted_token, R,
-                                                      (int)(row_bytes / 16), static_cast<uint4*>(xs));
+                                                      rows_dev, (int)(row_bytes / 16),
+                                                      static_cast<uint4*>(xs));
   else
     gather_rows_w4_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint32_t*>(x), sorted_token, R,
-                                                     (int)(row_bytes / 4), static_cast<uint32_t*>(xs));
+                                                     rows_dev, (int)(row_bytes / 4),
+                                                     static_cast<uint32_t*>(xs));
   return cudaGetLastError();
 }
 

@@ -36,6 +36,7 @@ __global__ void ffn_gateup_f32_kernel(const float* __restrict__ xs, const float*
     float* dst;
     if (i < n_routed) {
       const int row = (int)(i / F), f = (int)(i % F);
+      if (row >= offsets[E]) continue;  // past the rows dispatched under a capacity
       const int e = segment_of(offsets, E, row);
       a = xs + (size_t)row * d;
       wg = wgu + ((size_t)e * 2 * F + f) * d;
@@ -70,6 +71,7 @@ __global__ void ffn_down_f32_kernel(const float* __restrict__ h, const float* __
     const float* w;
     int K;
     if (row < R) {
+      if (row >= offsets[E]) continue;  // past the rows dispatched under a capacity
       const int e = segment_of(offsets, E, row);
       a = h + (size_t)row * F;
       w = wd + ((size_t)e * d + c) * F;

@@ -83,11 +83,15 @@ cudaError_t launch_topk(int src, const float* a, const float* b, const float* bi
 // Dispatch (moe_dispatch.cu).
 // ntp / ntp2 (either may be null): per-expert prefixes of tile units (seg_units) for n-tile
 // caps bn / bn2 and tall-tile limits 0 / tall2.
+// capacity: per-expert limit of dispatched assignments (INT_MAX: dropless); *dropped (may be
+// null) receives the number dropped; a dropped assignment gets slot_pos -1.
 cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
                             int* expert_counts, int* offsets, int* ntp, int bn2, int tall2,
-                            int* ntp2, int* sorted_token, int* slot_pos, cudaStream_t s);
-cudaError_t launch_gather(const void* x, const int* sorted_token, int R, int d, int elt_bytes,
-                          void* xs, cudaStream_t s);
+                            int* ntp2, int capacity, int* dropped, int* sorted_token,
+                            int* slot_pos, cudaStream_t s);
+// rows_dev (may be null): device row count replacing R (rows dispatched under a capacity).
+cudaError_t launch_gather(const void* x, const int* sorted_token, int R, const int* rows_dev,
+                          int d, int elt_bytes, void* xs, cudaStream_t s);
 
 // fp32 expert FFN on CUDA cores (moe_ffn_simt.cu).
 cudaError_t launch_ffn_f32(const float* xs, const float* x, const int* offsets, int E, int R,

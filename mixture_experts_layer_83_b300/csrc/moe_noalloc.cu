@@ -79,7 +79,7 @@ extern "C" int moe_route_from_keys_noalloc(const moe_shape* s, const float* sel_
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, scratch, expert_counts, expert_offsets,
-                      nullptr, 0, 0, nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
+                      nullptr, 0, 0, nullptr, INT_MAX, nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

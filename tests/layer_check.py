@@ -8,6 +8,9 @@ same inputs, and compare them the way the layer's correctness criteria read:
 * group-limited routing (a workload with ``topk_groups`` > 0 keeps that many of its ``groups``
   expert groups per token): the same, against the oracle's group-limited top-k, whose margin
   also covers near-ties between groups;
+* expert capacity (a workload with ``capacity_factor`` > 0): dispatch tables and the number
+  dropped bit-exactly against the oracle's capacity dispatch of the GPU's routing, and the
+  output against the oracle with the dropped assignments contributing nothing;
 * output: max |err| <= 2e-2 * max |ref| and sum |err| / sum |ref| <= 5e-3 for bf16 (tighter
   for fp32), the oracle evaluated under the GPU's routing, so an accepted near-tie does not
   count as an output error.
@@ -44,12 +47,16 @@ def gpu_forward(cfg, dev, stream=None, workspace=None, stage_events=None):
     tidx = torch.empty((T, k), dtype=torch.int32, device=out.device)
     tw = torch.empty((T, k), dtype=torch.float32, device=out.device)
     st = torch.empty(T * k, dtype=torch.int32, device=out.device)
+    dropped = torch.zeros(4, dtype=torch.int32, device=out.device)
     shared = (dev["sh_gate_up"], dev["sh_down"]) if c["Fs"] > 0 else None
+    cf = c.get("capacity_factor", 0.0)
     moe.moe_layer_forward(shape, dev["x"], dev["w_router"], dev["w_gate_up"], dev["w_down"],
                           c["score"], dev.get("bias"), shared, out, counts, workspace, ws_bytes,
-                          stream, tidx, tw, st, stage_events=stage_events, **group_args(c))
+                          stream, tidx, tw, st, stage_events=stage_events,
+                          capacity_factor=cf, dropped=dropped if cf > 0 else None,
+                          **group_args(c))
     return dict(out=out, counts=counts, topk_idx=tidx, topk_w=tw, sorted_token=st,
-                workspace=workspace)
+                dropped=dropped[:1], workspace=workspace)
 
 
 def to_host(res):
@@ -125,12 +132,23 @@ def check_routing(cfg, key, score, margin, o_idx, g_idx, g_w):
     return int(excluded.sum()), w_ref
 
 
-def check_dispatch(cfg, g_idx, g_counts, g_sorted):
+def check_dispatch(cfg, g_idx, g_counts, g_sorted, g_dropped=None):
+    """Dispatch tables of the GPU's routing against the oracle's; returns (counts, kept mask
+    [T][k]) -- the mask is all True for a dropless layer."""
     c = configs.get(cfg)
+    cf = c.get("capacity_factor", 0.0)
+    if cf > 0:
+        cap = oracle.capacity(c["T"], c["E"], c["k"], cf)
+        counts, offsets, st, sp, dropped = oracle.dispatch_capacity(g_idx.astype(np.int32),
+                                                                    c["E"], cap)
+        np.testing.assert_array_equal(g_counts, counts)
+        np.testing.assert_array_equal(g_sorted[:offsets[-1]], st)
+        assert g_dropped is not None and int(g_dropped[0]) == dropped
+        return counts, sp >= 0
     counts, offsets, st, _ = oracle.dispatch(g_idx.astype(np.int32), c["E"])
     np.testing.assert_array_equal(g_counts, counts)
     np.testing.assert_array_equal(g_sorted, st)
-    return counts
+    return counts, np.ones(g_idx.shape, dtype=bool)
 
 
 def check_output(cfg, got, ref):
@@ -167,7 +185,9 @@ def full_check(cfg, dev=None, host=None, threads=None):
     key, score, o_idx, margin = oracle_routing(c, host["x"], host["w_router"], host.get("bias"),
                                                threads)
     n_ex, w_ref = check_routing(c, key, score, margin, o_idx, res["topk_idx"], res["topk_w"])
-    check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"])
+    _, kept = check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"],
+                             res["dropped"])
+    w_ref = np.where(kept, w_ref, 0.0)   # a dropped assignment contributes nothing
     experts = {e: (host["w_gate_up"][e], host["w_down"][e]) for e in range(c["E"])}
     shared = (host["sh_gate_up"], host["sh_down"]) if c["Fs"] > 0 else None
     ref = oracle_rows(c, host["x"], res["topk_idx"], w_ref, experts, shared, threads)
@@ -201,7 +221,9 @@ def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
     bias = dev["bias"].cpu().numpy() if "bias" in dev else None
     key, score, o_idx, margin = oracle_routing(c, x, wr, bias, threads)
     n_ex, w_ref = check_routing(c, key, score, margin, o_idx, res["topk_idx"], res["topk_w"])
-    counts = check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"])
+    counts, kept = check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"],
+                                  res["dropped"])
+    w_ref = np.where(kept, w_ref, 0.0)   # a dropped assignment contributes nothing
     T, k = c["T"], c["k"]
     if n_sample >= T:
         sample = np.arange(T)
@@ -213,6 +235,8 @@ def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
         cold = int(np.argmin(np.where(counts > 0, counts, np.iinfo(np.int32).max)))
         for e in (hot, cold):
             sample.add(int(np.where((idx == e).any(1))[0][0]))
+        if not kept.all():   # and a token with a dropped assignment
+            sample.add(int(np.where(~kept.all(1))[0][-1]))
         sample = np.array(sorted(sample))
     n = sample.size
     g_idx = res["topk_idx"][sample]
@@ -241,7 +265,8 @@ def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
     ref = oracle.combine(slots, w_ref[sample], ys, y_sh)
     stats = check_output(c, res["out"][sample], ref)
     stats.update(excluded=n_ex, sampled=int(n), experts_touched=int((counts > 0).sum()),
-                 max_over_mean=float(counts.max() / counts.mean()))
+                 max_over_mean=float(counts.max() / counts.mean()),
+                 dropped=int((~kept).sum()))
     return stats
 
 

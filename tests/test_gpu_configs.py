@@ -42,3 +42,17 @@ def test_full_size_skewed_layer_with_group_limited_routing():
     print(c["name"], "group-limited", stats)
     del dev
     torch.cuda.empty_cache()
+
+
+def test_full_size_skewed_layer_with_capacity():
+    """The Zipf-skewed layer (hottest experts at about 16x the mean load) with a capacity
+    factor of 1.25: the hot experts overflow and their late tokens are dropped; dispatch
+    tables and the number dropped bit-exactly, sampled outputs with drops contributing nothing."""
+    c = dict(configs.CONFIGS[4], capacity_factor=1.25)
+    dev = moe_inputs.device_inputs(c)
+    torch.cuda.synchronize()
+    stats = sampled_check(c, dev, n_sample=SAMPLE[4])
+    print(c["name"], "capacity 1.25", stats)
+    assert stats["dropped"] > 0
+    del dev
+    torch.cuda.empty_cache()

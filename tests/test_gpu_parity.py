@@ -174,6 +174,35 @@ GROUPED = {
 }
 
 
+CAPACITY = {
+    # skewed by a large bias on two experts: they overflow a capacity of 1.0 x the mean load
+    "bf16_capacity_1.0": dict(make_shape(400, 256, 16, 4, 192, Fs=64, score=SIGMOID,
+                                         bias_range=0.01, seed=41), capacity_factor=1.0),
+    # softmax, fractional capacity (300 * 2 / 7 * 1.25 = 107.1 -> 108 slots)
+    "bf16_capacity_1.25": dict(make_shape(300, 192, 7, 2, 128, seed=42), capacity_factor=1.25),
+    # a tiny capacity: most assignments dropped, some tokens lose every expert
+    "bf16_capacity_tiny": dict(make_shape(200, 128, 8, 2, 64, seed=43), capacity_factor=0.05),
+    # fp32 layer with drops
+    "f32_capacity": dict(make_shape(99, 70, 5, 2, 33, Fs=17, dtype="f32", score=SIGMOID,
+                                    bias_range=0.05, seed=44), capacity_factor=0.8),
+    # group-limited routing and a capacity together
+    "bf16_groups_and_capacity": dict(make_shape(500, 256, 64, 8, 128, Fs=64, score=SIGMOID,
+                                                bias_range=0.01, seed=45), groups=8,
+                                     topk_groups=3, capacity_factor=1.1),
+}
+
+
+@pytest.mark.parametrize("name", list(CAPACITY))
+def test_capacity_layer_matches_oracle(name):
+    cfg = CAPACITY[name]
+    host = moe_inputs.host_inputs(cfg)
+    if name == "bf16_capacity_1.0":
+        host["bias"] = host["bias"].copy()
+        host["bias"][[3, 11]] = 0.5     # two hot experts
+    stats = full_check(cfg, host=host)
+    print(name, stats)
+
+
 @pytest.mark.parametrize("name", list(GROUPED))
 def test_group_limited_layer_matches_oracle(name):
     stats = full_check(GROUPED[name])
@@ -184,5 +213,5 @@ def test_forward_dispatch_tables_match_oracle_for_gpu_routing():
     cfg = SMALL["bf16_many_experts"]
     dev = moe_inputs.upload(cfg, moe_inputs.host_inputs(cfg))
     res = to_host(gpu_forward(cfg, dev))
-    counts = check_dispatch(cfg, res["topk_idx"], res["counts"], res["sorted_token"])
+    counts, _ = check_dispatch(cfg, res["topk_idx"], res["counts"], res["sorted_token"])
     assert counts.sum() == cfg["T"] * cfg["k"]
