@@ -178,13 +178,14 @@ class Runner:
         self.shared = (dev["sh_gate_up"], dev["sh_down"]) if c["Fs"] > 0 else None
         self.stream = torch.cuda.current_stream()
         self.launches = moe.moe_layer_num_launches(self.shape)
+        self.options = {}   # routing options of moe_layer_forward (group limits, capacity)
 
     def step(self, x=None, events=None):
         d = self.dev
         self.moe.moe_layer_forward(self.shape, d["x"] if x is None else x, d["w_router"],
                                    d["w_gate_up"], d["w_down"], self.c["score"], d.get("bias"),
                                    self.shared, self.out, self.counts, self.ws, self.ws_bytes,
-                                   self.stream, stage_events=events)
+                                   self.stream, stage_events=events, **self.options)
 
     def timed(self, steps, warmup, world, with_stages=True):
         torch = self.torch
@@ -386,6 +387,40 @@ def measure(c, args, world, rank, peaks, sampler, kind):
     return res
 
 
+def skew_report(args, world, rank):
+    """The Zipf-skewed layer: time per pass and the expert / group load (max over mean of the
+    dispatched assignments; the 8 contiguous groups of 16 experts stand for an expert-parallel
+    placement over 8 GPUs), dropless and under the two routing options that act on skew."""
+    import torch
+    c = configs.CONFIGS[4]
+    dev = rank_inputs(c, rank)
+    torch.cuda.synchronize()
+    r = Runner(c, dev)
+    dropped = torch.zeros(4, dtype=torch.int32, device="cuda")
+    groups = c["groups"]
+    res = {"workload": workload_config(c)["workload"],
+           "groups": f"{groups} contiguous groups of {c['E'] // groups} experts"}
+    variants = (("dropless", {}),
+                ("group_limited_4_of_8", dict(n_groups=groups, topk_groups=4)),
+                ("capacity_1.25", dict(capacity_factor=1.25, dropped=dropped)))
+    for name, opts in variants:
+        r.options = opts
+        ms, _, _ = r.timed(args.steps, args.warmup, world, with_stages=False)
+        counts = r.counts.cpu().numpy().astype(np.float64)
+        per_group = counts.reshape(groups, -1).sum(1)
+        entry = {"ms_per_step": ms, "tokens_per_s": c["T"] / (ms * 1e-3),
+                 "expert_max_over_mean": float(counts.max() / counts.mean()),
+                 "group_max_over_mean": float(per_group.max() / per_group.mean()),
+                 "experts_touched": int((counts > 0).sum())}
+        if "capacity_factor" in opts:
+            entry["dropped_assignments"] = int(dropped[0].item())
+            entry["dropped_fraction"] = int(dropped[0].item()) / (c["T"] * c["k"])
+        res[name] = entry
+    del r, dev
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,6 +468,9 @@ def main():
     del main_res["runner"], r
     torch.cuda.empty_cache()
     dec = measure(dc, args, world, rank, peaks, sampler, "decode")
+    del dec["runner"]
+    torch.cuda.empty_cache()
+    skew = skew_report(args, world, rank)
     if rank == 0:
         sampler.stop()
     if world > 1:
@@ -504,6 +542,7 @@ def main():
         "layer": main_res["layer"],
         "stages_ms": {n: float(v) for n, v in zip(names, st)},
         "decode": decode,
+        "skewed": skew,
     }
     print(json.dumps(line))
     if world > 1:
