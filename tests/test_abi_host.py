@@ -118,8 +118,9 @@ def _check_schedule(s, which, counts):
     # with a second one
     assert geo["smem_bytes"] <= (232448 if which == 0 or geo["bn"] > 256 else 114688)
     bn = geo["bn"]
-    # gate/up runs on wide CTA pairs (n-tiles up to 512 token rows), the others up to 256
-    assert bn % 16 == 0 and 16 <= bn <= (512 if which == 1 else 256)
+    # the expert GEMMs run on wide CTA pairs for long segments (n-tiles up to 384 token rows),
+    # the router up to 256
+    assert bn % 16 == 0 and 16 <= bn <= (384 if which > 0 else 256)
     if which == 0:
         seg_rows = [s.T]
         seg_off = [0, s.T]
@@ -206,7 +207,7 @@ def test_prefill_geometry_uses_full_width_tiles():
     assert geo["bn"] == 384 and geo["stages_a"] == 6 and geo["stages_b"] == 4
     assert geo["m_tiles0"] == 32 and geo["cg"] == 2
     _, geo = moe.moe_debug_gemm_tiles(s, 2, np.full(256, 256))
-    assert geo["bn"] == 256 and geo["stages_a"] == 4 and geo["stages_b"] == 2
+    assert geo["bn"] == 384 and geo["stages_a"] == 6 and geo["stages_b"] == 4
     assert geo["m_tiles0"] == 56 and geo["cg"] == 2
     _, geo = moe.moe_debug_gemm_tiles(shape(T=128, d=7168, E=256, k=8, F=2048, Fs=2048), 1,
                                       np.full(256, 4))
@@ -214,20 +215,22 @@ def test_prefill_geometry_uses_full_width_tiles():
     assert geo["bn"] == 32 and geo["stages_a"] == 4 and geo["stages_b"] == 8
 
 
-def test_gateup_tall_and_wide_tiles():
-    """Prefill gate/up: segments of up to 256 rows run as tall tiles (four weight tiles of 128
-    rows, i.e. two pairs, over all the segment's rows); longer ones as wide tiles (one pair over
-    up to 384 rows)."""
+@pytest.mark.parametrize("which,m_tiles", [(1, 32), (2, 56)])
+def test_prefill_expert_gemms_tall_and_wide_tiles(which, m_tiles):
+    """Prefill expert GEMMs: segments of up to 256 rows run as tall tiles (four weight tiles of
+    128 rows, i.e. two pairs, over all the segment's rows); longer ones as wide tiles (one pair
+    over up to 384 rows)."""
     s = shape(T=8192, d=7168, E=256, k=8, F=2048, Fs=2048)
     counts = np.full(256, 256)
     counts[1] = 300
     counts[2] = 0
     counts[3] = 10
-    tiles, geo = moe.moe_debug_gemm_tiles(s, 1, counts)
+    tiles, geo = moe.moe_debug_gemm_tiles(s, which, counts)
+    assert geo["m_tiles0"] == m_tiles
     routed = tiles[tiles[:, 0] == 0]
     for e, n in ((0, 256), (1, 300), (3, 10)):
         t = routed[routed[:, 1] == e]
-        assert len(t) == 32 and sorted(t[:, 2].tolist()) == list(range(32))
+        assert len(t) == m_tiles and sorted(t[:, 2].tolist()) == list(range(m_tiles))
         assert (t[:, 5] == n).all() and (t[:, 4] == (n + 15) // 16 * 16).all()
         if n <= 256:   # tall: the CTA tiles of one tile are four consecutive weight tiles
             assert (t[:, 2].reshape(-1, 4) == t[::4, 2:3] + np.arange(4)).all()
