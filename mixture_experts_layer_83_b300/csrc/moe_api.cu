@@ -140,10 +140,15 @@ int expert_bn(const moe_shape& s) {
 // two narrow pairs per TPC instead.
 bool gateup_wide(const moe_shape& s) { return expert_bn(s) >= 256; }
 
-// n-tile cap of the gate/up GEMM on wide pairs: 384 token rows (one pass over an expert's weights
-// for segments up to 384 rows; the cap leaves shared memory for a six-deep weight ring); the
-// down GEMM's cap otherwise.
-int gateup_bn(const moe_shape& s) { return gateup_wide(s) ? 384 : expert_bn(s); }
+// n-tile cap of the expert GEMMs on wide pairs: 512 token rows when experts average 384 rows or
+// more (two full 256-column MMA halves per tile), else 384 (segments near the mean still fit
+// one tile, and the smaller token stages leave shared memory for a six-deep weight ring); the
+// narrow cap otherwise.
+int gateup_bn(const moe_shape& s) {
+  if (!gateup_wide(s)) return expert_bn(s);
+  const long long R = (long long)s.T * s.k;
+  return (R + s.E - 1) / s.E >= 384 ? 512 : 384;
+}
 
 // Segments of at most 256 rows run on wide pairs as tall tiles: two scheduled m-tiles (512
 // weight rows per pair) over all the segment's rows, one per MMA issuer, which halves the
