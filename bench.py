@@ -387,6 +387,26 @@ def measure(c, args, world, rank, peaks, sampler, kind):
     return res
 
 
+def other_configs(args, world, rank, peaks):
+    """The tiny fp32 and the Mixtral-8x7B-shaped layers: time per pass and roofline fraction."""
+    import torch
+    out = {}
+    for cid in (0, 1):
+        c = configs.CONFIGS[cid]
+        res = measure(c, args, world, rank, peaks, None, c["name"])
+        out[c["name"]] = {"workload": workload_config(c)["workload"], "ms_per_step": res["ms"],
+                          "tokens_per_s": c["T"] * world / (res["ms"] * 1e-3),
+                          "layer": res["layer"],
+                          "stages_ms": {n: float(v) for n, v in
+                                        zip(res["runner"].moe.STAGE_NAMES, res["stages"])}}
+        if c["dtype"] != "bf16":
+            out[c["name"]]["note"] = ("true-fp32 CUDA-core path, launch-bound at this size: the "
+                                      "bf16 tensor roofline does not bound it")
+        del res
+        torch.cuda.empty_cache()
+    return out
+
+
 def skew_report(args, world, rank):
     """The Zipf-skewed layer: time per pass and the expert / group load (max over mean of the
     dispatched assignments; the 8 contiguous groups of 16 experts stand for an expert-parallel
@@ -471,6 +491,7 @@ def main():
     del dec["runner"]
     torch.cuda.empty_cache()
     skew = skew_report(args, world, rank)
+    others = other_configs(args, world, rank, peaks)
     if rank == 0:
         sampler.stop()
     if world > 1:
@@ -543,6 +564,7 @@ def main():
         "stages_ms": {n: float(v) for n, v in zip(names, st)},
         "decode": decode,
         "skewed": skew,
+        "other_configs": others,
     }
     print(json.dumps(line))
     if world > 1:

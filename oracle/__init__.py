@@ -57,13 +57,14 @@ def lib():
         l.oracle_topk_grouped.argtypes = [ci, ci, ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_dispatch.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_capacity.argtypes = [ci, ci, ci, ctypes.c_double]
+        l.oracle_eplb_plan.argtypes = [vp, ci, ci, ci, vp, vp, vp]
         l.oracle_dispatch_capacity.argtypes = [ci, ci, ci, vp, ci, vp, vp, vp, vp, vp]
         l.oracle_gather.argtypes = [ci, ci, vp, vp, vp]
         l.oracle_combine.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_swiglu_ffn.argtypes = [ci, ci, ci, vp, vp, vp, vp]
         l.oracle_layer_rows.argtypes = [ctypes.POINTER(OracleLayer), ci, vp, vp, vp, vp]
         for f in ("oracle_router_scores", "oracle_topk", "oracle_topk_grouped", "oracle_dispatch",
-                  "oracle_capacity", "oracle_dispatch_capacity",
+                  "oracle_capacity", "oracle_dispatch_capacity", "oracle_eplb_plan",
                   "oracle_gather",
                   "oracle_combine", "oracle_swiglu_ffn", "oracle_layer_rows"):
             getattr(l, f).restype = ci
@@ -151,6 +152,18 @@ def dispatch_capacity(topk_idx, E, cap):
                                           _p(offsets), _p(st), _p(sp), _p(dropped)),
            "dispatch_capacity")
     return counts, offsets, st[:offsets[-1]], sp, int(dropped[0])
+
+
+def eplb_plan(load, n_gpus, n_redundant):
+    """Expert placement with redundant experts (see moe_oracle.c):
+    (slot_expert, slot_gpu, gpu_load)."""
+    load = np.ascontiguousarray(load, dtype=np.int32)
+    S = load.size + n_redundant
+    se = np.empty(S, dtype=np.int32); sg = np.empty(S, dtype=np.int32)
+    gl = np.empty(n_gpus, dtype=np.float64)
+    _check(lib().oracle_eplb_plan(_p(load), load.size, n_gpus, n_redundant, _p(se), _p(sg),
+                                  _p(gl)), "eplb_plan")
+    return se, sg, gl
 
 
 def gather(sorted_token, x):

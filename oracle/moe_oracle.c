@@ -339,3 +339,84 @@ int oracle_layer_rows(const oracle_layer* L, int n_tok, const void* x_rows, cons
   free(y);
   return rc;
 }
+
+/* Expert placement with redundant experts (page "Expert-Parallel MoE Inference: Serving Sparse
+ * Models at Scale", section "Load imbalance and how to fight it": redundant experts duplicate
+ * the hottest experts so their load spreads; EPLB computes an expert-to-GPU placement that
+ * equalises expected load).  The pages give the goal, not the algorithm; the plain reading:
+ *   1. every expert has one replica; each of the n_redundant extra slots goes, one at a time, to
+ *      the expert with the largest load per replica (equal: the lower expert id); a replica
+ *      carries load / replicas;
+ *   2. replicas are placed largest first (equal loads: lower expert id, then lower replica
+ *      index), each on the GPU with the smallest load among those with a free slot and no
+ *      replica of the same expert (if every GPU with a free slot already holds one, among all
+ *      GPUs with a free slot); equal loads: the lower GPU id.  Each GPU has
+ *      (E + n_redundant) / n_gpus slots.
+ * slot_expert / slot_gpu [E + n_redundant]: slot s of GPU g is g * slots_per_gpu + (its order of
+ * placement on g); gpu_load [n_gpus]. */
+int oracle_eplb_plan(const int* load, int E, int n_gpus, int n_redundant, int* slot_expert,
+                     int* slot_gpu, double* gpu_load) {
+  if (!load || E < 1 || n_gpus < 1 || n_redundant < 0 || !slot_expert || !slot_gpu || !gpu_load)
+    return -1;
+  const int S = E + n_redundant;
+  if (S % n_gpus != 0) return -1;
+  const int per_gpu = S / n_gpus;
+  int* rep = (int*)calloc((size_t)E, sizeof(int));
+  int* item_e = (int*)malloc(sizeof(int) * (size_t)S);
+  int* item_r = (int*)malloc(sizeof(int) * (size_t)S);
+  char* used = (char*)calloc((size_t)S, 1);
+  int* filled = (int*)calloc((size_t)n_gpus, sizeof(int));
+  char* hosts = (char*)calloc((size_t)n_gpus * (size_t)E, 1);
+  if (!rep || !item_e || !item_r || !used || !filled || !hosts) {
+    free(rep); free(item_e); free(item_r); free(used); free(filled); free(hosts);
+    return -1;
+  }
+  for (int e = 0; e < E; ++e) {
+    if (load[e] < 0) { free(rep); free(item_e); free(item_r); free(used); free(filled); free(hosts); return -1; }
+    rep[e] = 1;
+  }
+  for (int r = 0; r < n_redundant; ++r) {
+    int best = 0;
+    for (int e = 1; e < E; ++e)
+      if ((double)load[e] / rep[e] > (double)load[best] / rep[best]) best = e;
+    rep[best] += 1;
+  }
+  int n = 0;
+  for (int e = 0; e < E; ++e)
+    for (int r = 0; r < rep[e]; ++r) {
+      item_e[n] = e;
+      item_r[n] = r;
+      ++n;
+    }
+  for (int g = 0; g < n_gpus; ++g) gpu_load[g] = 0.0;
+  for (int placed = 0; placed < S; ++placed) {
+    /* next item: the largest unplaced replica load; ties: lower expert, then lower replica */
+    int it = -1;
+    for (int i = 0; i < S; ++i) {
+      if (used[i]) continue;
+      if (it < 0) { it = i; continue; }
+      const double li = (double)load[item_e[i]] / rep[item_e[i]];
+      const double lt = (double)load[item_e[it]] / rep[item_e[it]];
+      if (li > lt || (li == lt && (item_e[i] < item_e[it] ||
+                                   (item_e[i] == item_e[it] && item_r[i] < item_r[it]))))
+        it = i;
+    }
+    used[it] = 1;
+    const int e = item_e[it];
+    int g_best = -1;
+    for (int pass = 0; pass < 2 && g_best < 0; ++pass)
+      for (int g = 0; g < n_gpus; ++g) {
+        if (filled[g] == per_gpu) continue;
+        if (pass == 0 && hosts[(size_t)g * E + e]) continue;
+        if (g_best < 0 || gpu_load[g] < gpu_load[g_best]) g_best = g;
+      }
+    const int slot = g_best * per_gpu + filled[g_best];
+    slot_expert[slot] = e;
+    slot_gpu[slot] = g_best;
+    filled[g_best] += 1;
+    hosts[(size_t)g_best * E + e] = 1;
+    gpu_load[g_best] += (double)load[e] / rep[e];
+  }
+  free(rep); free(item_e); free(item_r); free(used); free(filled); free(hosts);
+  return 0;
+}

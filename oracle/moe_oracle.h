@@ -111,6 +111,11 @@ typedef struct {
 int oracle_layer_rows(const oracle_layer* L, int n_tok, const void* x_rows, const int* topk_idx,
                       const double* topk_w, double* out);
 
+/* Expert placement over n_gpus GPUs with n_redundant extra replicas of the hottest experts
+ * (see moe_oracle.c): slot_expert / slot_gpu [E + n_redundant], gpu_load [n_gpus]. */
+int oracle_eplb_plan(const int* load, int E, int n_gpus, int n_redundant, int* slot_expert,
+                     int* slot_gpu, double* gpu_load);
+
 #ifdef __cplusplus
 }
 #endif

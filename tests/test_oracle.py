@@ -341,6 +341,59 @@ def test_combine_skips_dropped_assignments():
     np.testing.assert_allclose(out, kept_w[:, None] * x, rtol=1e-14, atol=1e-14)
 
 
+# ------------------------------------------------------------------ redundant-expert placement
+def test_eplb_hand_cases():
+    """8 experts with loads [10,1,...,1] on 2 GPUs.  No replicas: the largest goes first to GPU 0,
+    GPU 1 fills its 4 slots with four 1s, GPU 0 takes the last three -> loads [13, 4].  Two
+    redundant slots: expert 0 takes both (10/1, then 10/2 lead), three replicas of 10/3; GPU 1
+    takes the second (GPU 0 already holds expert 0), the third goes back to GPU 0 (both hold one,
+    equal load, lower id), GPU 1 then takes four 1s and GPU 0 the last three -> [29/3, 22/3]."""
+    se, sg, gl = oracle.eplb_plan([10, 1, 1, 1, 1, 1, 1, 1], 2, 0)
+    np.testing.assert_array_equal(gl, [13.0, 4.0])
+    assert se.tolist() == [0, 5, 6, 7, 1, 2, 3, 4] and sg.tolist() == [0] * 4 + [1] * 4
+    se, sg, gl = oracle.eplb_plan([10, 1, 1, 1, 1, 1, 1, 1], 2, 2)
+    np.testing.assert_allclose(gl, [29 / 3, 22 / 3], rtol=1e-15)
+    assert se.tolist() == [0, 0, 5, 6, 7, 0, 1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("E,G,R", [(16, 4, 0), (16, 4, 4), (128, 8, 8), (256, 16, 16), (10, 5, 5)])
+def test_eplb_invariants(E, G, R):
+    """Skewed random loads: every expert placed at least once, each GPU exactly (E+R)/G slots,
+    load conserved, a GPU holds two replicas of an expert only if some GPU holds none of it is
+    impossible (more replicas than GPUs), and the replicated experts are those the greedy
+    favours: an expert a with n_a >= 2 replicas had the largest load per replica when it got its
+    last one, i.e. load_a / (n_a - 1) >= load_b / n_b for every other expert b."""
+    rng = np.random.default_rng(E + G + R)
+    load = (rng.pareto(1.2, E) * 100).astype(np.int32)
+    se, sg, gl = oracle.eplb_plan(load, G, R)
+    S = E + R
+    assert sorted(set(se.tolist())) == list(range(E))
+    assert np.bincount(sg, minlength=G).tolist() == [S // G] * G
+    n = np.bincount(se, minlength=E)
+    np.testing.assert_allclose(gl.sum(), load.sum(), rtol=1e-12)
+    per = load / n
+    np.testing.assert_allclose(np.bincount(sg, weights=per[se], minlength=G), gl, rtol=1e-12)
+    for a in np.where(n >= 2)[0]:
+        assert load[a] / (n[a] - 1) >= (per[np.arange(E) != a]).max() - 1e-9
+    for g in range(G):
+        held = se[sg == g]
+        for e in set(held.tolist()):
+            if (held == e).sum() > 1:
+                assert n[e] > G
+
+
+def test_eplb_balances_a_skewed_load():
+    """A Zipf-like load on 64 experts over 8 GPUs: the plan's max/mean GPU load is below the
+    contiguous placement's and falls further with redundant slots."""
+    load = (1000 * np.arange(1, 65) ** -1.2).astype(np.int32)
+    contiguous = load.reshape(8, 8).sum(1)
+    ratio = lambda gl: gl.max() / gl.mean()
+    r0 = ratio(contiguous)
+    r1 = ratio(oracle.eplb_plan(load, 8, 0)[2])
+    r2 = ratio(oracle.eplb_plan(load, 8, 8)[2])
+    assert r0 > r1 > r2 >= 1.0
+
+
 def test_identity_experts_round_trip_returns_x():
     """Dispatch (gather) then combine with identity experts returns x (weights sum to 1)."""
     rng = np.random.default_rng(5)
