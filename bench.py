@@ -407,6 +407,21 @@ def other_configs(args, world, rank, peaks):
     return out
 
 
+def eplb_report(counts, n_gpus):
+    """The library's replica plan on this pass's expert counts: per-GPU expected load, max over
+    mean, for the contiguous placement and for plans with 0, 1 and 4 redundant slots per GPU."""
+    import mixture_experts_layer_83_b300 as moe
+    contiguous = counts.reshape(n_gpus, -1).sum(1)
+    out = {"gpus": n_gpus, "contiguous_max_over_mean": float(contiguous.max() / contiguous.mean())}
+    for per_gpu in (0, 1, 4):
+        t0 = time.perf_counter()
+        _, _, gl = moe.moe_eplb_plan(counts, n_gpus, per_gpu * n_gpus)
+        out[f"plan_redundant_{per_gpu * n_gpus}"] = {
+            "gpu_max_over_mean": float(gl.max() / gl.mean()),
+            "plan_us": (time.perf_counter() - t0) * 1e6}
+    return out
+
+
 def skew_report(args, world, rank):
     """The Zipf-skewed layer: time per pass and the expert / group load (max over mean of the
     dispatched assignments; the 8 contiguous groups of 16 experts stand for an expert-parallel
@@ -435,6 +450,8 @@ def skew_report(args, world, rank):
         if "capacity_factor" in opts:
             entry["dropped_assignments"] = int(dropped[0].item())
             entry["dropped_fraction"] = int(dropped[0].item()) / (c["T"] * c["k"])
+        if name == "dropless":
+            entry["eplb"] = eplb_report(counts.astype(np.int32), groups)
         res[name] = entry
     del r, dev
     torch.cuda.empty_cache()

@@ -26,9 +26,9 @@
  *      floating-point atomics, so the output is bit-reproducible from run to run (page "MoE
  *      Expert Parallelism in Practice", "Core Principles" part 1: outputs are combined and
  *      mapped back to the original token order).
- * The layer is drop-free: every assignment is computed (page "Expert-Parallel MoE
- * Inference", "Capacity factor and token dropping": production inference prefers a
- * drop-free path).
+ * The layer is drop-free unless the caller sets an expert capacity (moe_forward_opts): every
+ * assignment is computed (page "Expert-Parallel MoE Inference", "Capacity factor and token
+ * dropping": production inference prefers a drop-free path).
  *
  * Conventions for every entry point:
  *   - Every array pointer is DEVICE memory owned by the caller, 16-byte aligned, row-major.
@@ -198,6 +198,26 @@ int moe_route_from_keys_noalloc(const moe_shape* s, const float* sel_key,
  * Returns the number of CTA tiles (may exceed max_tiles) or a negative MOE_ERR_*. */
 int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,
                          int* tiles, int max_tiles, int* geometry);
+
+/* Redundant-expert placement plan, HOST code: every pointer is HOST memory, nothing is
+ * enqueued.  Pages "Expert-Parallel MoE Inference: Serving Sparse Models at Scale", section
+ * "Load imbalance and how to fight it", and "Tensor vs Expert vs Data Parallelism for MoE
+ * Serving", section "Load imbalance and EPLB": copies of hot experts in n_redundant extra slots
+ * and an expert-to-GPU placement that evens the expected per-GPU load.
+ *   expert_load [E] int32 >= 0, e.g. expert_counts summed over recent steps
+ *   slot_expert [E + n_redundant], slot_gpu [E + n_redundant]: written; slot i holds a replica
+ *     of expert slot_expert[i] on GPU slot_gpu[i]; GPU g owns slots g*P .. g*P + P - 1,
+ *     P = (E + n_redundant) / n_gpus, filled in placement order
+ *   gpu_load [n_gpus] fp64: written; the expected load of each GPU, a replica of expert e
+ *     carrying expert_load[e] / (replicas of e)
+ * The plan: each redundant slot goes to the expert with the largest load per replica (equal:
+ * lower id); replicas, largest load per replica first (equal: lower expert, lower replica), go
+ * to the least-loaded GPU with a free slot that does not yet hold the expert, else to the
+ * least-loaded GPU with a free slot (equal load: lower GPU id).  Every expert gets at least one
+ * slot and every GPU exactly P.  MOE_ERR_INVALID_ARG for a null pointer, E < 1, n_gpus < 1,
+ * n_redundant < 0, E + n_redundant > 2^20 or not a multiple of n_gpus, or a negative load. */
+int moe_eplb_plan(const int* expert_load, int E, int n_gpus, int n_redundant, int* slot_expert,
+                  int* slot_gpu, double* gpu_load);
 
 /* Kernel launches one moe_layer_forward makes for this shape (for launch accounting). */
 int moe_layer_num_launches(const moe_shape* s);

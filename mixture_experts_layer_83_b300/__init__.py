@@ -27,7 +27,7 @@ STAGE_NAMES = ("router_gemm", "topk", "dispatch", "gather", "gateup_gemm", "down
 
 EXPORTED = ("moe_layer_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
             "moe_route_from_keys", "moe_route_from_keys_grouped", "moe_route_from_keys_noalloc",
-            "moe_debug_gemm_tiles",
+            "moe_debug_gemm_tiles", "moe_eplb_plan",
             "moe_layer_num_launches", "moe_workspace_status", "moe_status_string")
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -83,6 +83,8 @@ def lib():
         l.moe_route_from_keys_noalloc.restype = ci
         l.moe_debug_gemm_tiles.argtypes = [shp, ci, ci, vp, vp, ci, vp]
         l.moe_debug_gemm_tiles.restype = ci
+        l.moe_eplb_plan.argtypes = [vp, ci, ci, ci, vp, vp, vp]
+        l.moe_eplb_plan.restype = ci
         l.moe_layer_num_launches.argtypes = [shp]
         l.moe_layer_num_launches.restype = ci
         l.moe_workspace_status.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -231,6 +233,22 @@ def moe_debug_gemm_tiles(shape, which, expert_counts=None, num_sms=148):
     keys = ("bn", "stages_a", "stages_b", "smem_bytes", "m_tiles0", "m_tiles1", "group", "K0",
             "cg")
     return tiles[:n], dict(zip(keys, (int(v) for v in geo)))
+
+
+def moe_eplb_plan(expert_load, n_gpus, n_redundant=0):
+    """Redundant-expert placement plan (host): returns (slot_expert [S] int32, slot_gpu [S]
+    int32, gpu_load [n_gpus] float64), S = E + n_redundant."""
+    import numpy as np
+    load = np.ascontiguousarray(expert_load, np.int32)
+    S = load.size + int(n_redundant)
+    se = np.zeros(max(S, 1), np.int32)
+    sg = np.zeros(max(S, 1), np.int32)
+    gl = np.zeros(max(int(n_gpus), 1), np.float64)
+    rc = lib().moe_eplb_plan(load.ctypes.data, load.size, int(n_gpus), int(n_redundant),
+                             se.ctypes.data, sg.ctypes.data, gl.ctypes.data)
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_eplb_plan")
+    return se[:S], sg[:S], gl[:int(n_gpus)]
 
 
 def moe_workspace_status(workspace):
