@@ -35,7 +35,8 @@
 //                              up rows; both are staged token-major in shared memory, then
 //                              each thread forms h = silu(gate) * up for 8 features of one
 //                              token and stores them as one 16-byte bf16 vector
-//                     down   : y staged token-major (bf16), stored as full 16-byte rows
+//                     down   : y (bf16) stored from registers, a warp's 32 channels of one
+//                              token per store
 // The tile scheduler reads the segment offsets and the n-tile prefix the dispatch scan wrote,
 // so nothing crosses to the host.  Tile order within a segment is (m-group, m, n-tile), so the
 // CTAs running at the same time share weight tiles (all n-tiles of an m) and token tiles (a
@@ -97,9 +98,7 @@ __device__ __forceinline__ NSplit n_split(int ncols) {
 }
 constexpr int kABytes = 128 * 128;       // weight stage: 128 rows x 64 bf16
 constexpr int kStageLdF = 68;            // fp32 row of the gate/up staging (64 + pad)
-constexpr int kStageLdH = 136;           // bf16 row of the down staging (128 + pad)
-constexpr int kXchgFloats = 2 * 16 * kStageLdF;  // 8704 B, also holds 32 x kStageLdH bf16
-static_assert(32 * kStageLdH * 2 <= kXchgFloats * 4, "down staging fits the epilogue buffer");
+constexpr int kXchgFloats = 2 * 16 * kStageLdF;  // 8704 B: gate and up, 16 tokens each
 constexpr int kBarBytes = 512;           // 2 * (12 + 8) + 6 mbarriers, rounded
 static_assert(8 * (2 * (kMaxStagesA + kMaxStagesB) + 6) <= kBarBytes, "mbarriers fit");
 constexpr int kMiscBytes = 128;
@@ -107,6 +106,18 @@ constexpr size_t kSmemLimit = 232448;    // 227 KiB opt-in per CTA
 constexpr size_t kSmemLimitPair = 112 * 1024;  // two per SM with room to spare in its 228 KiB
 constexpr size_t kSmemFloor = 120 * 1024;  // keeps a second one-CTA kernel (and its TMEM demand) off the SM
 size_t smem_limit(int cg, int wide) { return cg == 2 && !wide ? kSmemLimitPair : kSmemLimit; }
+
+// One lane's output channel for up to 32 tokens (rows ld apart), fp32 accumulators to bf16.
+__device__ __forceinline__ void store_down_chunk(__nv_bfloat16* y, int ld, int n, const uint32_t (&v)[32]) {
+  if (n >= 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[(size_t)j * ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) y[(size_t)j * ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
+  }
+}
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -525,28 +536,28 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
           }
         }
       } else if (MODE == kModeDown) {
-        // Per 32 tokens: each lane writes its channel's 32 values (bf16) token-major into
-        // shared memory; then the 128 threads store full 256-byte y rows in 16-byte vectors.
-        __nv_bfloat16* ys = reinterpret_cast<__nv_bfloat16*>(xchg);  // [32][kStageLdH]
-        const int chl = q * 32 + lane;
-        __nv_bfloat16* yout = static_cast<__nv_bfloat16*>(P.out);
-        for (int c = 0; c < nchunks; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c * 32), v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ys[j * kStageLdH + chl] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          named_bar_sync(bar_sync, 128);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int idx = i * 128 + ep;
-            const int tok = idx >> 4, part = idx & 15;
-            const int col = c * 32 + tok;
-            const int ch0 = tl.m * 128 + part * 8;
-            if (col < valid && ch0 < P.out_valid_m)
-              *reinterpret_cast<uint4*>(yout + (size_t)(rowb + col) * P.out_ld + ch0) =
-                  *reinterpret_cast<const uint4*>(ys + tok * kStageLdH + part * 8);
+        // Lane = output channel, register j = token 32c + j: for each token the warp stores its
+        // 32 consecutive channels (64 contiguous bytes) straight from registers, with no
+        // shared-memory transpose and no group barrier.  The tensor-memory load of the next
+        // chunk is in flight while one is stored.
+        const int ch = tl.m * 128 + q * 32 + lane;
+        __nv_bfloat16* ycol = static_cast<__nv_bfloat16*>(P.out) + (size_t)rowb * P.out_ld + ch;
+        const bool ch_ok = ch < P.out_valid_m;
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32_issue(tbase, va);
+        tmem_ld_wait(va);
+        for (int c = 0; c < nchunks; c += 2) {  // nchunks is uniform over the group
+          const bool more = c + 1 < nchunks;
+          if (more) tmem_ld_32x32b_x32_issue(tbase + static_cast<uint32_t>((c + 1) * 32), vb);
+          if (ch_ok) store_down_chunk(ycol + (size_t)(c * 32) * P.out_ld, P.out_ld, valid - c * 32, va);
+          if (more) {
+            tmem_ld_wait(vb);
+            const bool again = c + 2 < nchunks;
+            if (again) tmem_ld_32x32b_x32_issue(tbase + static_cast<uint32_t>((c + 2) * 32), va);
+            if (ch_ok)
+              store_down_chunk(ycol + (size_t)((c + 1) * 32) * P.out_ld, P.out_ld, valid - (c + 1) * 32, vb);
+            if (again) tmem_ld_wait(va);
           }
-          named_bar_sync(bar_sync, 128);
         }
       } else {
         const int e = tl.m * 128 + q * 32 + lane;
