@@ -33,7 +33,7 @@ CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 # oracle sample sizes (tokens) giving roughly 10-30 s of single-core fp64 work
-CPU_SAMPLE = {0: 64, 1: 16, 2: 12, 3: 12, 4: 32}
+CPU_SAMPLE = {0: 64, 1: 8, 2: 12, 3: 12, 4: 16}
 REF_SAMPLE = {0: 64, 1: 4, 2: 3, 3: 3, 4: 8}
 
 
@@ -319,6 +319,18 @@ def cpu_oracle_sample(c, dev, ntok, rank_seed_note=""):
     return ntok / dt, dt
 
 
+def cpu_baseline_entry(args, world, rank, c, dev):
+    """The oracle timed on a bounded sample of config ``c`` (rank 0 of a one-GPU run only)."""
+    if args.no_cpu_baseline or world != 1 or rank != 0:
+        return None
+    n = next(CPU_SAMPLE[i] for i, x in configs.CONFIGS.items() if x["name"] == c["name"])
+    v, dt = cpu_oracle_sample(c, dev, n)
+    return {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} tokens of the {c['name']} batch: router, top-k, routed "
+                      f"experts{', shared expert' if c['Fs'] > 0 else ''}, combine in fp64 "
+                      f"({dt:.1f} s)"}
+
+
 def run_reference(args, c):
     world, rank, local = dist_info()
     if rank != 0:
@@ -402,6 +414,7 @@ def other_configs(args, world, rank, peaks):
         if c["dtype"] != "bf16":
             out[c["name"]]["note"] = ("true-fp32 CUDA-core path, launch-bound at this size: the "
                                       "bf16 tensor roofline does not bound it")
+        out[c["name"]]["cpu_baseline"] = cpu_baseline_entry(args, world, rank, c, res["dev"])
         del res
         torch.cuda.empty_cache()
     return out
@@ -453,6 +466,7 @@ def skew_report(args, world, rank):
         if name == "dropless":
             entry["eplb"] = eplb_report(counts.astype(np.int32), groups)
         res[name] = entry
+    res["cpu_baseline"] = cpu_baseline_entry(args, world, rank, c, dev)
     del r, dev
     torch.cuda.empty_cache()
     return res
@@ -557,13 +571,8 @@ def main():
                            "peak_source": f"{peak_src} HBM copy"},
               "experts_touched": int((dec["counts"] > 0).sum())}
 
-    cpu = None
-    if not args.no_cpu_baseline:
-        n = CPU_SAMPLE[args.config]
-        v, dt = cpu_oracle_sample(c, main_res["dev"], n)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {n} tokens of the {c['name']} batch: router, top-k, routed and "
-                         f"shared experts, combine in fp64 ({dt:.1f} s)"}
+    cpu = cpu_baseline_entry(args, world, rank, c, main_res["dev"])
+    decode["cpu_baseline"] = cpu_baseline_entry(args, world, rank, dc, dec["dev"])
     line = {
         "metric": "MoE-layer tokens/s, DeepSeek-V3 shape (T=8192 prefill; T=128 decode under "
                   "'decode')",
