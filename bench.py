@@ -273,19 +273,30 @@ class Runner:
         return ms, h2d, d2h
 
 
-def traffic_record(kernel):
-    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source is unchanged."""
+def code_digest(files):
+    """sha256 of C/C++/CUDA sources with comments and blank lines removed: a change to the code
+    changes it, an edit of comments alone does not."""
     import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in files:
+        text = open(os.path.join(ROOT, f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
+    return h.hexdigest()
+
+
+def traffic_record(kernel):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel code is unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(kernel)
     if not rec:
         return None
-    h = hashlib.sha256()
-    for f in rec.get("sources", []):
-        h.update(open(os.path.join(ROOT, f), "rb").read())
-    return rec["bytes_per_launch"] if h.hexdigest() == rec.get("sha256") else None
+    return rec["bytes_per_launch"] if code_digest(rec.get("sources", [])) == rec.get("sha256") else None
 
 
 def cpu_oracle_sample(c, dev, ntok, rank_seed_note=""):

@@ -1,8 +1,8 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) for sm_103a.
 //
-// Computes D = A * B^T per tile, A = weight rows (the MMA's M), B = up to 256 token rows (the
-// MMA's N, any multiple of 16), K in 64-element blocks; bf16 operands, fp32 accumulation in
-// tensor memory.  Putting the weights on M and the tokens on N ("swap AB") lets a tile follow
+// Computes D = A * B^T per tile, A = weight rows (the MMA's M), B = token rows (the MMA's N,
+// any multiple of 16 up to 256 per MMA; a wide tile runs two MMAs over up to 512), K in
+// 64-element blocks; bf16 operands, fp32 accumulation in tensor memory.  Putting the weights on M and the tokens on N ("swap AB") lets a tile follow
 // an expert's token count with 16-row granularity, so a ragged expert segment wastes at most
 // 15 rows -- the same kernel serves 256-row prefill segments and 4-row decode segments.  The
 // experts run as one grouped GEMM over the expert segments (page "Tensor vs Expert vs Data
@@ -20,15 +20,17 @@
 //           CTAs' barriers (multicast).
 //
 // Roles (persistent over a static tile stride; warps 0..6, plus warps 7..11 for a wide pair,
-// plus extra producer warps for the pair forms):
+// plus extra producer warps for the pair forms; warp 7 of a wide pair is the second MMA
+// issuer and warps 8..11 the second epilogue group, each owning one accumulator half):
 //   warp 0 lane 0   weight producer: TMA of the 128 x 64 weight block of each k-step into
 //                   the weight ring (16 KiB stages, up to 12 deep): weights come from HBM
 //                   and need the longest look-ahead
 //   warp 6 lane 0   token producer: TMA of this CTA's N (or N/2) x 64 token block into the
 //                   token ring (token tiles are L2 hits, re-read by every weight tile)
 //   warp 1 lane 0   MMA issuer (even CTA of a pair only): 4 x tcgen05.mma (K=16) per k-step
-//                   into one of two TMEM accumulators (256 columns each); commits release ring
-//                   stages and hand finished accumulators to the epilogues
+//                   into a TMEM accumulator (two 256-column buffers for the one-CTA form, one
+//                   per pair otherwise); commits release ring stages and hand finished
+//                   accumulators to the epilogues
 //   warps 2..5      epilogue: tcgen05.ld, then per mode
 //                     router : fp32 logits [T][E]
 //                     gate/up: rows 0..63 of the CTA's A are gate rows, 64..127 the matching
@@ -60,14 +62,18 @@ constexpr int kMaxStagesB = 8;
 constexpr int kAccCols = 256;  // one accumulator: 128 lanes x up to 256 fp32 columns
 // Three forms share this kernel:
 //   one CTA (CG = 1, router): one CTA per SM, accumulator double-buffered in 512 TMEM columns.
-//   narrow pair (CG = 2, down): two pairs per TPC (two CTAs per SM), one 256-column
-//     accumulator each; the second pair keeps the tensor cores busy while the first drains its
-//     accumulator, and two MMA issuers per SM halve the per-instruction issue cost (about 125
-//     cycles per tcgen05.mma from one thread) that otherwise bounds MMAs with N < 256.
-//   wide pair (CG = 2, WIDE, gate/up): one pair per TPC, n-tiles of up to 512 token rows in one
-//     512-column accumulator, split over two MMA issuers (one per 256-column half) and two
-//     epilogue groups.  An expert's whole token segment (up to 512 rows) shares one pass over
-//     its weights, so each weight tile is streamed from HBM once.
+//   narrow pair (CG = 2, both expert GEMMs at decode-sized segments, n-tile cap under 256
+//     rows): two pairs per TPC (two CTAs per SM), one 256-column accumulator each; the second
+//     pair keeps the tensor cores busy while the first drains its accumulator, and two MMA
+//     issuers per SM halve the per-instruction issue cost (about 125 cycles per tcgen05.mma
+//     from one thread) that otherwise bounds MMAs with N < 256.
+//   wide pair (CG = 2, WIDE, both expert GEMMs at prefill-sized segments): one pair per TPC,
+//     n-tiles of up to 512 token rows in one 512-column accumulator, split over two MMA
+//     issuers (one per 256-column half) and two epilogue groups.  An expert's whole token
+//     segment (up to 512 rows) shares one pass over its weights, so each weight tile is
+//     streamed from HBM once.  A segment of at most 256 rows runs as a tall tile instead: two
+//     scheduled m-tiles over all of its rows, each issuer and epilogue group taking one m-tile,
+//     so both issuers still run MMAs with N = the segment's rows.
 // Producer threads per ring.  One thread's TMA issue bounds the stream it keeps in flight, so
 // the pair forms spread each ring over several producer warps.  Producer pid owns the ring
 // stages s with s % producers == pid and fills their rounds in order: every stage keeps a
