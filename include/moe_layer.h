@@ -188,13 +188,15 @@ int moe_route_from_keys_noalloc(const moe_shape* s, const float* sel_key,
  * (0 = router, 1 = gate/up, 2 = down) would run for the given per-expert token counts
  * (host array [E]; ignored for the router) on a device with num_sms SMs.  Writes up to
  * max_tiles rows of 7 ints, one per CTA tile, {operand set (0 routed / 1 shared), segment,
- * 128-row weight tile m, first token row, MMA N, rows that belong to the segment, loads
- * second 64-row weight box} into tiles (host; may be NULL), and 9 ints {n-tile cap,
+ * 128-row weight tile m, first token row, token columns N (a multiple of 16; over 256 they are
+ * split across two MMAs), rows that belong to the segment, loads second 64-row weight box}
+ * into tiles (host; may be NULL), and 9 ints {n-tile cap,
  * weight-ring stages, token-ring stages, shared-memory bytes per CTA, weight tiles of set 0,
  * weight tiles of set 1, m-group, K of set 0, CTAs per MMA (1, or 2 for a CTA pair)} into
  * geometry (host, may be NULL).  In the CTA-pair GEMMs (gate/up and down) the two CTAs of a
  * pair hold weight tiles 2j and 2j + 1 over the same token rows; the second is listed only
- * when it exists.
+ * when it exists.  A tall tile (a segment short enough for one n-tile, on the wide pair form)
+ * covers two scheduled weight tiles: its CTA tiles 4j .. 4j + 3 are listed in that order.
  * Returns the number of CTA tiles (may exceed max_tiles) or a negative MOE_ERR_*. */
 int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,
                          int* tiles, int max_tiles, int* geometry);
