@@ -60,3 +60,15 @@ def test_byte_model_counts_only_touched_experts():
     s = 2
     want = 2 * 128 * 7168 * s + 256 * 7168 * s + 10 * 3 * 7168 * 2048 * s + 3 * 7168 * 2048 * s
     assert bench.layer_bytes(c, counts) == want
+
+
+def test_code_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  /* store */\n}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    a = bench.code_digest(["k.cu"])
+    src.write_text("// another header\n\n__global__ void k(int* p) {\n  p[0] = 1;\n}\n// end\n")
+    assert bench.code_digest(["k.cu"]) == a
+    src.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
+    assert bench.code_digest(["k.cu"]) != a
+
