@@ -205,16 +205,110 @@ def _host_elems(t):
     return t.cpu().numpy()
 
 
-def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
+def _cta_box_edges(g0, rows):
+    """Rows on both sides of each TMA box edge of one CTA's token rows [g0, g0 + rows): the
+    kernel covers them with boxes of 128, 64, 32, 16 and 8 rows."""
+    edges, off = [], 0
+    for box in (128, 64, 32, 16, 8):
+        n = (rows - off) // box if box == 128 else (1 if rows - off >= box else 0)
+        for _ in range(n):
+            off += box
+            edges += [g0 + off - 1, g0 + off]
+    return edges
+
+
+def tile_edge_rows(row0, ncols, valid, wide):
+    """Token rows of a GEMM tile where its index arithmetic changes: the first and last valid
+    rows, the split of each MMA's N rows over the two CTAs of a pair, the split of a wide tile
+    into its two MMAs (n0 = the first half rounded up to 16 rows) and the TMA box edges."""
+    rows = [row0, row0 + valid - 1]
+    if wide and ncols > 256:
+        n0 = (((ncols >> 4) + 1) >> 1) << 4
+        halves = [(row0, n0), (row0 + n0, ncols - n0)]
+    else:
+        halves = [(row0, ncols)]
+    for start, n in halves:
+        rows += [start - 1, start, start + n // 2 - 1, start + n // 2, start + n - 1]
+        rows += _cta_box_edges(start, n // 2) + _cta_box_edges(start + n // 2, n // 2)
+    return [r for r in rows if row0 <= r < row0 + valid]
+
+
+def boundary_tokens(cfg, counts, sorted_token):
+    """Tokens whose rows sit on tile edges of the two expert GEMMs, from the kernels' own tile
+    decoder (moe_debug_gemm_tiles): every edge of every n-tile and tall tile of the hottest,
+    the coldest and a median non-empty expert, the last row of every expert's segment, and the
+    edges of the shared expert's first and last n-tiles.  Returns (tokens, description)."""
+    import mixture_experts_layer_83_b300 as moe
+    c = configs.get(cfg)
+    shape = moe.make_shape(c["T"], c["d"], c["E"], c["k"], c["F"], c["Fs"], moe_dtype(c))
+    counts = np.asarray(counts, dtype=np.int32)
+    nz = np.where(counts > 0)[0]
+    by_count = nz[np.argsort(counts[nz], kind="stable")]
+    picked = {int(by_count[-1]), int(by_count[0]), int(by_count[len(by_count) // 2])}
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    rows, sh_tokens = set(), set()
+    tiles_seen = 0
+    for which in (1, 2):
+        tiles, geo = moe.moe_debug_gemm_tiles(shape, which, counts)
+        wide = geo["bn"] > 256
+        for prob, seg, _m, row0, ncols, valid, _b in tiles.tolist():
+            if prob == 0 and seg in picked:
+                rows.update(tile_edge_rows(row0, ncols, valid, wide))
+                tiles_seen += 1
+        sh = tiles[tiles[:, 0] == 1]
+        if sh.size:
+            for row0 in (int(sh[:, 3].min()), int(sh[:, 3].max())):
+                t = sh[sh[:, 3] == row0][0]
+                sh_tokens.update(tile_edge_rows(int(t[3]), int(t[4]), int(t[5]), wide))
+    rows.update(int(offsets[e + 1] - 1) for e in nz)      # each segment's last row
+    toks = {int(sorted_token[r]) for r in rows} | sh_tokens
+    desc = dict(experts=sorted(picked), tile_rows=len(rows), shared_rows=len(sh_tokens),
+                tiles=tiles_seen)
+    return toks, desc
+
+
+def _oracle_expert_rows(dev, xs64, by_expert, threads):
+    """ys[(i, j)] for every sampled (token row i, slot j) grouped by expert: each expert's
+    weights are copied to the host once and its pairs are spread over host threads; an
+    expert's host copy is released when its last pair is done."""
+    import threading
+    from concurrent.futures import ThreadPoolExecutor
+    total = sum(len(v) for v in by_expert.values())
+    chunk = max(1, -(-total // (4 * threads)))
+    tasks = [(e, pairs[i:i + chunk]) for e, pairs in sorted(by_expert.items())
+             for i in range(0, len(pairs), chunk)]
+    left = {e: -(-len(p) // chunk) for e, p in by_expert.items()}
+    cache, locks, mu = {}, {e: threading.Lock() for e in by_expert}, threading.Lock()
+    out = {}
+
+    def run(task):
+        e, pairs = task
+        with locks[e]:
+            if e not in cache:
+                cache[e] = (_host_elems(dev["w_gate_up"][e]), _host_elems(dev["w_down"][e]))
+            wgu, wd = cache[e]
+        res = [((i, j), oracle.swiglu_ffn(xs64[i], wgu, wd)) for i, j in pairs]
+        with mu:
+            out.update(res)
+            left[e] -= 1
+            if left[e] == 0:
+                cache.pop(e, None)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, tasks))
+    return out
+
+
+def sampled_check(cfg, dev, n_sample=1024, threads=None, seed=0):
     """Full-size check: the whole layer runs on the GPU as bench.py runs it; routing is checked
-    for every token, dispatch tables bit-exactly, outputs on a seeded sample of tokens (plus
-    the first token of the hottest and of the coldest non-empty expert).  The oracle evaluates
-    each sampled (token, expert) pair with its SwiGLU and sums them with its combine; expert
-    weights are copied to the host one expert at a time."""
+    for every token, dispatch tables bit-exactly, outputs on a seeded sample of ``n_sample``
+    tokens plus every token on a tile edge of the expert GEMMs (boundary_tokens) and, under a
+    capacity, a token with a dropped assignment.  The oracle evaluates each sampled (token,
+    expert) pair with its SwiGLU and sums them with its combine."""
     from concurrent.futures import ThreadPoolExecutor
     import os
     c = configs.get(cfg)
-    threads = threads or max(1, os.cpu_count() or 1)
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
     res = to_host(gpu_forward(c, dev))
     x = _host_elems(dev["x"])
     wr = _host_elems(dev["w_router"])
@@ -225,36 +319,30 @@ def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
                                   res["dropped"])
     w_ref = np.where(kept, w_ref, 0.0)   # a dropped assignment contributes nothing
     T, k = c["T"], c["k"]
+    edges = {}
     if n_sample >= T:
         sample = np.arange(T)
     else:
         rng = np.random.default_rng(seed)
         sample = set(rng.choice(T, n_sample, replace=False).tolist())
-        idx = res["topk_idx"]
-        hot = int(np.argmax(counts))
-        cold = int(np.argmin(np.where(counts > 0, counts, np.iinfo(np.int32).max)))
-        for e in (hot, cold):
-            sample.add(int(np.where((idx == e).any(1))[0][0]))
+        forced = set()
+        if c["dtype"] == "bf16":
+            forced, edges = boundary_tokens(c, counts, res["sorted_token"])
         if not kept.all():   # and a token with a dropped assignment
-            sample.add(int(np.where(~kept.all(1))[0][-1]))
-        sample = np.array(sorted(sample))
+            forced.add(int(np.where(~kept.all(1))[0][-1]))
+        edges["forced_tokens"] = len(forced - sample)
+        sample = np.array(sorted(sample | forced))
     n = sample.size
     g_idx = res["topk_idx"][sample]
     xs64 = as_float64(c, x[sample])
-    ys = np.zeros((n * k, c["d"]))
     by_expert = {}
     for i in range(n):
         for j in range(k):
             by_expert.setdefault(int(g_idx[i, j]), []).append((i, j))
-
-    def run_expert(e):
-        wgu = _host_elems(dev["w_gate_up"][e])
-        wd = _host_elems(dev["w_down"][e])
-        for i, j in by_expert[e]:
-            ys[i * k + j] = oracle.swiglu_ffn(xs64[i], wgu, wd)
-
-    with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(run_expert, sorted(by_expert)))
+    yd = _oracle_expert_rows(dev, xs64, by_expert, threads)
+    ys = np.zeros((n * k, c["d"]))
+    for (i, j), y in yd.items():
+        ys[i * k + j] = y
     y_sh = None
     if c["Fs"] > 0:
         shg, shd = _host_elems(dev["sh_gate_up"]), _host_elems(dev["sh_down"])
@@ -266,7 +354,7 @@ def sampled_check(cfg, dev, n_sample=64, threads=None, seed=0):
     stats = check_output(c, res["out"][sample], ref)
     stats.update(excluded=n_ex, sampled=int(n), experts_touched=int((counts > 0).sum()),
                  max_over_mean=float(counts.max() / counts.mean()),
-                 dropped=int((~kept).sum()))
+                 dropped=int((~kept).sum()), edges=edges)
     return stats
 
 

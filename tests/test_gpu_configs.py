@@ -1,6 +1,7 @@
 """Parity at the five full-size workloads, in the configuration bench.py times (device-resident
 seeded inputs, one moe_layer_forward call): routing for every token, dispatch tables
-bit-exactly, layer outputs on sampled tokens (all tokens for the tiny and decode layers)."""
+bit-exactly, layer outputs on 1024 sampled tokens plus every token on a tile edge of the
+expert GEMMs (all tokens for the tiny and decode layers)."""
 import pytest
 
 import moe_inputs
@@ -11,7 +12,7 @@ from layer_check import sampled_check
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-SAMPLE = {0: 64, 1: 48, 2: 48, 3: 128, 4: 64}
+SAMPLE = {0: 64, 1: 1024, 2: 1024, 3: 128, 4: 1024}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -27,6 +28,8 @@ def test_full_size_config(cfg_id):
     torch.cuda.synchronize()
     stats = sampled_check(c, dev, n_sample=SAMPLE[cfg_id])
     print(c["name"], stats)
+    if SAMPLE[cfg_id] < c["T"] and c["dtype"] == "bf16":
+        assert stats["sampled"] >= SAMPLE[cfg_id] and stats["edges"]["tile_rows"] > 0
     del dev
     torch.cuda.empty_cache()
 
