@@ -34,6 +34,9 @@ CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 # oracle sample sizes (tokens) giving roughly 10-30 s of single-core fp64 work
 CPU_SAMPLE = {0: 64, 1: 8, 2: 12, 3: 12, 4: 16}
+# the one metric string both arms print (the reference arm is the fp64 oracle on host cores)
+METRIC = ("MoE-layer tokens/s, DeepSeek-V3 shape (T=8192 prefill; T=128 decode under "
+          "'decode')")
 REF_SAMPLE = {0: 64, 1: 4, 2: 3, 3: 3, 4: 8}
 
 
@@ -107,7 +110,7 @@ class ClockSampler:
             try:
                 ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
-                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10], float(f[4])))
             except (ValueError, IndexError):
                 continue
         if not rows:
@@ -121,7 +124,10 @@ class ClockSampler:
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
         out = {"sm_mhz": float(np.median([r[1] for r in inside])),
                "sm_max_mhz": float(max(r[2] for r in inside)), "reasons": reasons,
-               "samples": len(inside)}
+               "samples": len(inside),
+               "power_w_median": float(np.median([r[4] for r in inside])),
+               "power_w_max": float(max(r[4] for r in inside)),
+               "sw_power_cap_samples": sum(1 for r in inside if r[3][3] == "Active")}
         if note:
             out["note"] = note
         return out
@@ -336,7 +342,7 @@ def cpu_baseline_entry(args, world, rank, c, dev):
         return None
     n = next(CPU_SAMPLE[i] for i, x in configs.CONFIGS.items() if x["name"] == c["name"])
     v, dt = cpu_oracle_sample(c, dev, n)
-    return {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", **host_cores(),
             "sample": f"first {n} tokens of the {c['name']} batch: router, top-k, routed "
                       f"experts{', shared expert' if c['Fs'] > 0 else ''}, combine in fp64 "
                       f"({dt:.1f} s)"}
@@ -357,18 +363,28 @@ def run_reference(args, c):
     times = [cpu_oracle_sample(c, dev, n)[1] for _ in range(args.steps)]
     t = float(np.sum(times))
     value = n * args.steps / t
-    line = {"impl": "reference", "metric": "MoE-layer tokens/s (fp64 CPU oracle)", "value": value,
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1000 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(c),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             **host_cores(),
                              "sample": f"{n} tokens per step (first {n} of the batch), router + "
                                        f"top-k + routed and shared experts + combine"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def host_cores():
+    """The host's core counts, stated beside the single-threaded oracle's figure."""
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except AttributeError:
+        usable = os.cpu_count()
+    return {"host_nproc": os.cpu_count(), "host_cores_usable": usable}
 
 
 def workload_config(c):
@@ -392,22 +408,28 @@ def measure(c, args, world, rank, peaks, sampler, kind):
     counts = r.counts.cpu().numpy()
     res = {"ms": ms_max, "ms_local": ms, "stages": stages, "t0": t0, "t1": t1, "counts": counts,
            "runner": r, "dev": dev}
+    res["layer"] = layer_roofline(c, counts, ms_max, peaks)
+    return res
+
+
+def layer_roofline(c, counts, ms, peaks):
+    """Layer roofline: t_roof = max(FLOPs / bf16 peak, bytes / HBM peak) over the step time.
+    The timed region is a fraction of a second of back-to-back passes, which runs at the
+    maximum SM clock (the clock record of the run shows it), so the peak is the measured
+    burst bf16 figure; the fraction against the sustained (seconds-long, power-capped) figure
+    is given beside it as context only."""
     fl = layer_flops(c)
     by = layer_bytes(c, counts)
-    # The layer runs as back-to-back passes (a long step under the power cap), so compute is
-    # bounded by the sustained bf16 figure; the burst-based roofline is reported beside it.
     t_mem = by / (peaks["hbm_gbs"] * 1e9)
-    t_roof = max(fl / (peaks["bf16_tflops_sustained"] * 1e12), t_mem)
-    t_roof_burst = max(fl / (peaks["bf16_tflops"] * 1e12), t_mem)
-    res["layer"] = {"tflops": fl / (ms_max * 1e-3) / 1e12, "gbs": by / (ms_max * 1e-3) / 1e9,
-                    "flop": fl, "bytes": by, "roofline_ms": t_roof * 1e3,
-                    "roofline_frac": t_roof * 1e3 / ms_max,
-                    "roofline_ms_burst": t_roof_burst * 1e3,
-                    "roofline_frac_burst": t_roof_burst * 1e3 / ms_max,
-                    "roofline_peaks": "bf16 sustained (burst beside it) and HBM copy, measured",
-                    "bound": "tensor" if fl / (peaks["bf16_tflops_sustained"] * 1e12) >= t_mem
-                    else "hbm"}
-    return res
+    t_tc = fl / (peaks["bf16_tflops"] * 1e12)
+    t_roof = max(t_tc, t_mem)
+    t_roof_sus = max(fl / (peaks["bf16_tflops_sustained"] * 1e12), t_mem)
+    return {"tflops": fl / (ms * 1e-3) / 1e12, "gbs": by / (ms * 1e-3) / 1e9,
+            "flop": fl, "bytes": by, "roofline_ms": t_roof * 1e3,
+            "roofline_frac": t_roof * 1e3 / ms,
+            "roofline_peaks": "bf16 burst and HBM copy, measured",
+            "bound": "tensor" if t_tc >= t_mem else "hbm",
+            "context_roofline_frac_at_sustained_bf16": t_roof_sus * 1e3 / ms}
 
 
 def other_configs(args, world, rank, peaks):
@@ -465,12 +487,12 @@ def skew_report(args, world, rank):
     for name, opts in variants:
         r.options = opts
         ms, _, _ = r.timed(args.steps, args.warmup, world, with_stages=False)
-        counts = r.counts.cpu().numpy().astype(np.float64)
-        per_group = counts.reshape(groups, -1).sum(1)
+        counts = r.counts.cpu().numpy()
+        load = r.moe.moe_load_report(counts, groups)
         entry = {"ms_per_step": ms, "tokens_per_s": c["T"] / (ms * 1e-3),
-                 "expert_max_over_mean": float(counts.max() / counts.mean()),
-                 "group_max_over_mean": float(per_group.max() / per_group.mean()),
-                 "experts_touched": int((counts > 0).sum())}
+                 "expert_max_over_mean": load["expert_max_over_mean"],
+                 "group_max_over_mean": load["group_max_over_mean"],
+                 "experts_touched": load["experts_touched"]}
         if "capacity_factor" in opts:
             entry["dropped_assignments"] = int(dropped[0].item())
             entry["dropped_fraction"] = int(dropped[0].item()) / (c["T"] * c["k"])
@@ -553,26 +575,34 @@ def main():
     gu_fl = gateup_flops(c)
     achieved = gu_fl / (gu_ms * 1e-3) / 1e12
     traffic = traffic_record("gemm_gateup_prefill")
-    # the gate/up GEMM is timed inside a long step (the timed passes run back to back under
-    # the power cap): its peak is the sustained bf16 figure; the burst fraction is beside it
-    roof = {"kernel": "gemm_tc_kernel<1,2,1> gate/up + SwiGLU (tcgen05, wide CTA pairs)",
-            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
-            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
-            "traffic": traffic,
-            "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step of "
-                           f"{args.steps} back-to-back passes)",
-            "frac_of_burst": achieved / peaks["bf16_tflops"], "burst_peak": peaks["bf16_tflops"],
-            "algorithmic_flop_per_launch": gu_fl, "ms_per_launch": gu_ms}
     clocks = sampler.summary(min(main_res["t0"], dec["t0"]), max(main_res["t1"], dec["t1"]))
+    # The timed region is a fraction of a second of back-to-back passes at the maximum SM
+    # clock (see "clocks"), so the gate/up GEMM's peak is the measured burst bf16 figure.  The
+    # fraction of the sustained (seconds-long, power-capped) figure is context only.
+    roof = {"kernel": "gemm_tc_kernel<1,2,1> gate/up + SwiGLU (tcgen05, wide CTA pairs)",
+            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "traffic": traffic,
+            "peak_source": f"{peak_src} bf16 burst (timed region {ms * args.steps:.0f} ms of "
+                           f"{args.steps} back-to-back passes)",
+            "algorithmic_flop_per_launch": gu_fl, "ms_per_launch": gu_ms,
+            "sm_mhz_median": clocks.get("sm_mhz"),
+            "ms_x_ghz": gu_ms * clocks["sm_mhz"] / 1e3 if clocks.get("sm_mhz") else None,
+            "context_frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
 
     dms = dec["ms"]
     dst = dec["stages"]
     d_gu_ms = float(dst[names.index("gateup_gemm")])
     d_dn_ms = float(dst[names.index("down_gemm")])
     d_gu_bytes = gateup_weight_bytes(dc, dec["counts"])
-    decode = {"workload": workload_config(dc)["workload"], "value": dc["T"] * world / (dms * 1e-3),
-              "unit": "tokens/s", "ms_per_step": dms, "layer": dec["layer"],
+    d_dn_bytes = d_gu_bytes // 2   # down weights: d x F per touched expert (+ the shared one)
+    # summary keys last, so that they survive in the end of the printed line
+    decode = {"workload": workload_config(dc)["workload"],
               "stages_ms": {n: float(v) for n, v in zip(names, dst)},
+              "cpu_baseline": cpu_baseline_entry(args, world, rank, dc, dec["dev"]),
+              "experts_touched": int((dec["counts"] > 0).sum()),
+              "down_gemm_hbm_frac": d_dn_bytes / (d_dn_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+              "layer": dec["layer"],
               "roofline": {"kernel": "gemm_tc_kernel<1,2,0> gate/up + SwiGLU (tcgen05, narrow CTA "
                                      "pairs)", "bound": "hbm",
                            "achieved": d_gu_bytes / (d_gu_ms * 1e-3) / 1e9,
@@ -580,13 +610,12 @@ def main():
                            "frac": d_gu_bytes / (d_gu_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                            "traffic": traffic_record("gemm_gateup_decode"),
                            "peak_source": f"{peak_src} HBM copy"},
-              "experts_touched": int((dec["counts"] > 0).sum())}
+              "unit": "tokens/s", "value": dc["T"] * world / (dms * 1e-3), "ms_per_step": dms,
+              "layer_roofline_frac": dec["layer"]["roofline_frac"]}
 
     cpu = cpu_baseline_entry(args, world, rank, c, main_res["dev"])
-    decode["cpu_baseline"] = cpu_baseline_entry(args, world, rank, dc, dec["dev"])
     line = {
-        "metric": "MoE-layer tokens/s, DeepSeek-V3 shape (T=8192 prefill; T=128 decode under "
-                  "'decode')",
+        "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(c),
@@ -599,9 +628,10 @@ def main():
         "clocks": clocks,
         "layer": main_res["layer"],
         "stages_ms": {n: float(v) for n, v in zip(names, st)},
-        "decode": decode,
-        "skewed": skew,
         "other_configs": others,
+        # kept last: a reader that keeps only the end of the line still sees these two
+        "skewed": skew,
+        "decode": decode,
     }
     print(json.dumps(line))
     if world > 1:

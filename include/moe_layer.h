@@ -112,7 +112,8 @@ int moe_layer_forward(const moe_shape* s, const void* x, const void* w_router,
                       int* sorted_token_out);
 
 /* Number of CUDA events moe_layer_forward_ex records when stage_events is given:
- * [0] start, [1] router GEMM, [2] top-k, [3] histogram/scan/permutation, [4] gather,
+ * [0] start, [1] router GEMM, [2] top-k, [3] histogram/scan/permutation, [4] gather (fp32
+ * layers only; a bf16 layer's gate/up GEMM gathers its token rows itself, so [4] == [3]),
  * [5] gate/up grouped GEMM, [6] down grouped GEMM, [7] combine (each after its kernels). */
 #define MOE_NUM_STAGE_EVENTS 8
 
@@ -175,7 +176,9 @@ int moe_route_from_keys_grouped(const moe_shape* s, const float* sel_key,
  * the library until the process exits.  Shapes whose histogram ((T*k + 1023)/1024 chunks x E
  * int32) does not fit are rejected with MOE_ERR_WORKSPACE before anything is enqueued.
  * The first call on a device looks up the array's device address (with that device
- * current); make that first call before any stream capture.  Every call on a device shares
+ * current); make that first call before any stream capture.  The address belongs to the
+ * device's context: after a device reset the next call looks it up again, so make that call
+ * before any capture too.  Every call on a device shares
  * the array, so calls whose work overlaps on the GPU race and must be serialised by the
  * caller.  No memory is allocated or freed. */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
@@ -201,6 +204,23 @@ int moe_route_from_keys_noalloc(const moe_shape* s, const float* sel_key,
 int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* expert_counts,
                          int* tiles, int max_tiles, int* geometry);
 
+/* Diagnostics of the device error path (the pages' "fixed buffers fail loudly", page "Tensor vs
+ * Expert vs Data Parallelism for MoE Serving", section "Trade-offs, Gotchas, and What Goes
+ * Wrong": a failure must surface as an error, never as a hang).  Both clear the status word at
+ * the start of `workspace` (the word moe_workspace_status reads), then enqueue on `stream` one
+ * launch that ends by itself and leaves the GPU usable:
+ *   moe_debug_unclustered_pair: the CTA-pair expert GEMM launched as two plain CTAs (no 2-CTA
+ *     cluster); it records code 5 and returns before touching shared or tensor memory.
+ *   moe_debug_wait_timeout: one CTA waits on an mbarrier that nothing completes, with a
+ *     wall-clock limit of limit_ns (1e3 .. 1e9 ns, else MOE_ERR_INVALID_ARG); when the limit
+ *     runs out it records code 6 and returns.
+ * Afterwards moe_workspace_status gives MOE_ERR_DEVICE with that code as the detail.  Device
+ * codes: 1 a producer's wait, 2 an MMA issuer's wait, 3 an epilogue's wait, 4 the final drain
+ * of in-flight copies ran out (limit 2 s each); 5 a pair kernel without clusters; 6 the
+ * diagnostic wait. */
+int moe_debug_unclustered_pair(void* workspace, cudaStream_t stream);
+int moe_debug_wait_timeout(void* workspace, unsigned long long limit_ns, cudaStream_t stream);
+
 /* Redundant-expert placement plan, HOST code: every pointer is HOST memory, nothing is
  * enqueued.  Pages "Expert-Parallel MoE Inference: Serving Sparse Models at Scale", section
  * "Load imbalance and how to fight it", and "Tensor vs Expert vs Data Parallelism for MoE
@@ -221,6 +241,24 @@ int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* 
 int moe_eplb_plan(const int* expert_load, int E, int n_gpus, int n_redundant, int* slot_expert,
                   int* slot_gpu, double* gpu_load);
 
+/* Load arithmetic, HOST code (host pointers, nothing enqueued).
+ * moe_load_expectation: expected rows per expert under uniform routing when n_gpus GPUs each
+ *   bring tokens_per_gpu tokens to one expert-parallel group (page "Tensor vs Expert vs Data
+ *   Parallelism for MoE Serving", sections "Why sparsity demands a large batch" and "A
+ *   back-of-envelope sizing helper"): *tokens_per_expert = tokens_per_gpu * n_gpus * k / E and
+ *   *slots_per_gpu = (E + n_redundant) / n_gpus.  n_gpus = 1 gives one GPU's batch * k / E.
+ * moe_load_report: from expert_counts [E] (e.g. a forward pass's, copied to the host), with
+ *   the experts in n_groups contiguous groups (an expert-parallel placement; E divisible by
+ *   n_groups): report[0] = mean rows per expert, report[1] = max / mean over experts,
+ *   report[2] = max / mean over groups (page "Expert-Parallel MoE Inference: Serving Sparse
+ *   Models at Scale", section "A capacity and throughput worked example": the busiest GPU's
+ *   load over the mean), report[3] = experts with at least one row.
+ * Both return MOE_OK, or MOE_ERR_INVALID_ARG for a null pointer, a size out of range (k > E,
+ * a negative count) or E not divisible by n_groups. */
+int moe_load_expectation(int tokens_per_gpu, int E, int k, int n_gpus, int n_redundant,
+                         double* slots_per_gpu, double* tokens_per_expert);
+int moe_load_report(const int* expert_counts, int E, int n_groups, double* report);
+
 /* Kernel launches one moe_layer_forward makes for this shape (for launch accounting). */
 int moe_layer_num_launches(const moe_shape* s);
 
@@ -228,6 +266,10 @@ int moe_layer_num_launches(const moe_shape* s);
  * SYNCHRONOUS (cudaMemcpy).  *status = MOE_OK, or MOE_ERR_DEVICE if a kernel gave up on an
  * internal wait; *detail = the raw code the kernel recorded (0 if none). */
 int moe_workspace_status(const void* workspace, int* status, int* detail);
+
+/* Name of the CUDA error (e.g. "cudaErrorInvalidConfiguration") behind the latest
+ * MOE_ERR_CUDA a launch returned on the calling host thread, "cudaSuccess" if none. */
+const char* moe_last_cuda_error_name(void);
 
 /* Static string for a status code. */
 const char* moe_status_string(int status);

@@ -27,8 +27,10 @@ STAGE_NAMES = ("router_gemm", "topk", "dispatch", "gather", "gateup_gemm", "down
 
 EXPORTED = ("moe_layer_workspace_size", "moe_layer_forward", "moe_layer_forward_ex",
             "moe_route_from_keys", "moe_route_from_keys_grouped", "moe_route_from_keys_noalloc",
-            "moe_debug_gemm_tiles", "moe_eplb_plan",
-            "moe_layer_num_launches", "moe_workspace_status", "moe_status_string")
+            "moe_debug_gemm_tiles", "moe_debug_unclustered_pair", "moe_debug_wait_timeout",
+            "moe_eplb_plan", "moe_load_expectation", "moe_load_report",
+            "moe_layer_num_launches", "moe_workspace_status", "moe_status_string",
+            "moe_last_cuda_error_name")
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
@@ -50,7 +52,8 @@ class MoeForwardOpts(ctypes.Structure):
 
 class MoeError(RuntimeError):
     def __init__(self, code, what):
-        super().__init__(f"{what}: {moe_status_string(code)} ({code})")
+        detail = f", {moe_last_cuda_error_name()}" if code == MOE_ERR_CUDA else ""
+        super().__init__(f"{what}: {moe_status_string(code)} ({code}{detail})")
         self.code = code
 
 
@@ -83,12 +86,23 @@ def lib():
         l.moe_route_from_keys_noalloc.restype = ci
         l.moe_debug_gemm_tiles.argtypes = [shp, ci, ci, vp, vp, ci, vp]
         l.moe_debug_gemm_tiles.restype = ci
+        l.moe_debug_unclustered_pair.argtypes = [vp, vp]
+        l.moe_debug_unclustered_pair.restype = ci
+        l.moe_debug_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
+        l.moe_debug_wait_timeout.restype = ci
         l.moe_eplb_plan.argtypes = [vp, ci, ci, ci, vp, vp, vp]
         l.moe_eplb_plan.restype = ci
+        dp = ctypes.POINTER(ctypes.c_double)
+        l.moe_load_expectation.argtypes = [ci, ci, ci, ci, ci, dp, dp]
+        l.moe_load_expectation.restype = ci
+        l.moe_load_report.argtypes = [vp, ci, ci, vp]
+        l.moe_load_report.restype = ci
         l.moe_layer_num_launches.argtypes = [shp]
         l.moe_layer_num_launches.restype = ci
         l.moe_workspace_status.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci)]
         l.moe_workspace_status.restype = ci
+        l.moe_last_cuda_error_name.argtypes = []
+        l.moe_last_cuda_error_name.restype = ctypes.c_char_p
         l.moe_status_string.argtypes = [ci]
         l.moe_status_string.restype = ctypes.c_char_p
         _lib = l
@@ -114,6 +128,10 @@ def _stream(stream):
 
 def make_shape(T, d, E, k, F, Fs=0, dtype=MOE_DTYPE_BF16):
     return MoeShape(T, d, E, k, F, Fs, dtype)
+
+
+def moe_last_cuda_error_name():
+    return lib().moe_last_cuda_error_name().decode()
 
 
 def moe_status_string(code):
@@ -235,6 +253,22 @@ def moe_debug_gemm_tiles(shape, which, expert_counts=None, num_sms=148):
     return tiles[:n], dict(zip(keys, (int(v) for v in geo)))
 
 
+def moe_debug_unclustered_pair(workspace, stream=None, check=True):
+    """Launch the CTA-pair GEMM without clusters (it records device code 5 and returns)."""
+    rc = lib().moe_debug_unclustered_pair(_ptr(workspace), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoeError(rc, "moe_debug_unclustered_pair")
+    return rc
+
+
+def moe_debug_wait_timeout(workspace, limit_ns, stream=None, check=True):
+    """Launch a wait that nothing completes, limited to ``limit_ns`` (records device code 6)."""
+    rc = lib().moe_debug_wait_timeout(_ptr(workspace), int(limit_ns), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoeError(rc, "moe_debug_wait_timeout")
+    return rc
+
+
 def moe_eplb_plan(expert_load, n_gpus, n_redundant=0):
     """Redundant-expert placement plan (host): returns (slot_expert [S] int32, slot_gpu [S]
     int32, gpu_load [n_gpus] float64), S = E + n_redundant."""
@@ -249,6 +283,29 @@ def moe_eplb_plan(expert_load, n_gpus, n_redundant=0):
     if rc != MOE_OK:
         raise MoeError(rc, "moe_eplb_plan")
     return se[:S], sg[:S], gl[:int(n_gpus)]
+
+
+def moe_load_expectation(tokens_per_gpu, E, k, n_gpus=1, n_redundant=0):
+    """(expert slots per GPU, expected rows per expert) under uniform routing (host)."""
+    slots, tpe = ctypes.c_double(0), ctypes.c_double(0)
+    rc = lib().moe_load_expectation(int(tokens_per_gpu), int(E), int(k), int(n_gpus),
+                                    int(n_redundant), ctypes.byref(slots), ctypes.byref(tpe))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_load_expectation")
+    return slots.value, tpe.value
+
+
+def moe_load_report(expert_counts, n_groups=1):
+    """Load statistics of host expert counts: dict with mean rows per expert, max/mean over
+    experts, max/mean over n_groups contiguous groups and the experts touched."""
+    import numpy as np
+    counts = np.ascontiguousarray(expert_counts, np.int32)
+    rep = np.zeros(4, np.float64)
+    rc = lib().moe_load_report(counts.ctypes.data, counts.size, int(n_groups), rep.ctypes.data)
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_load_report")
+    return {"mean_rows_per_expert": float(rep[0]), "expert_max_over_mean": float(rep[1]),
+            "group_max_over_mean": float(rep[2]), "experts_touched": int(rep[3])}
 
 
 def moe_workspace_status(workspace):

@@ -28,6 +28,14 @@ constexpr int kMaxK = 32;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The CUDA error behind this thread's latest MOE_ERR_CUDA (moe_last_cuda_error_name).
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+int cuda_failed(cudaError_t e) {
+  t_last_cuda_error = e;
+  return MOE_ERR_CUDA;
+}
+
 struct Layout {
   size_t status, logits, topk_idx, topk_w, chunk, offsets, ntp, ntp2, sorted, slot, xs_y, h, h_sh, total;
 };
@@ -140,24 +148,46 @@ int expert_bn(const moe_shape& s) {
 // two narrow pairs per TPC instead.
 bool gateup_wide(const moe_shape& s) { return expert_bn(s) >= 256; }
 
-// n-tile cap of the expert GEMMs on wide pairs: 512 token rows when experts average 384 rows or
-// more (two full 256-column MMA halves per tile), else 384 (segments near the mean still fit
-// one tile, and the smaller token stages leave shared memory for a six-deep weight ring); the
-// narrow cap otherwise.
-int gateup_bn(const moe_shape& s) {
-  if (!gateup_wide(s)) return expert_bn(s);
-  const long long R = (long long)s.T * s.k;
-  return (R + s.E - 1) / s.E >= 384 ? 512 : 384;
-}
-
-// Segments of at most 256 rows run on wide pairs as tall tiles: two scheduled m-tiles (512
-// weight rows per pair) over all the segment's rows, one per MMA issuer, which halves the
-// token traffic per FLOP and gives both issuers full-width MMAs.  Needs an even number of
-// scheduled m-tiles.
+// Segments run on wide pairs as tall tiles: two scheduled m-tiles (512 weight rows per pair)
+// over up to 256 of the segment's rows, one per MMA issuer, which halves the token traffic
+// per FLOP against a 256-row weight tile and gives both issuers full-width MMAs.  Needs an
+// even number of scheduled m-tiles.
 int gateup_tall_rows(const moe_shape& s) {
   const int pairs = (s.F / 64 + 1) / 2;
   return gateup_wide(s) && pairs % 2 == 0 ? 256 : 0;
 }
+
+// Whether every segment runs as tall n-tiles (ceil(rows / 256) of them, rows split evenly):
+// the n-tile cap is then the tall-tile limit.  Chosen when experts average 384 rows or more:
+// long segments then stream each token stage once per 512 weight rows instead of 256
+// (measured on one B300, same box: Mixtral-shaped layer 2.10 ms against 2.24 ms with wide
+// tiles); at about 256 rows per expert (the DeepSeek-V3 prefill layer) the wide tiles of up
+// to 384 rows are faster (7.39 ms against 7.96 ms).
+bool gateup_all_tall(const moe_shape& s) {
+  const long long R = (long long)s.T * s.k;
+  return gateup_tall_rows(s) > 0 && (R + s.E - 1) / s.E >= 384;
+}
+
+// n-tile cap of the expert GEMMs on wide pairs: the tall-tile limit when every tile is tall;
+// else 512 token rows when experts average 384 rows or more (two full 256-column MMA halves
+// per tile), else 384 (segments near the mean still fit one tile, and the smaller token stages
+// leave shared memory for a six-deep weight ring); the narrow cap otherwise.
+int gateup_bn(const moe_shape& s) {
+  if (!gateup_wide(s)) return expert_bn(s);
+  if (gateup_all_tall(s)) return gateup_tall_rows(s);
+  const long long R = (long long)s.T * s.k;
+  return (R + s.E - 1) / s.E >= 384 ? 512 : 384;
+}
+
+// Whether the gate/up GEMM gathers its token rows from x itself (TMA tile::gather4 through
+// the dispatch permutation: the fused dispatch) instead of reading a permuted copy of x that a
+// separate gather kernel writes.  It does on narrow pairs (decode-sized segments), where the
+// gathers cost nothing measurable and the gather launch goes away.  Wide pairs need a token
+// stage of up to 256 rows per CTA every k-step, 64 four-row gathers against 2 box loads, and
+// the TMA unit's gather rate then bounds the GEMM below its tensor rate (measured on one B300,
+// same box, DeepSeek-V3 prefill: gate/up 4.93 ms gathering against 4.28 ms + 0.25 ms for the
+// separate gather).
+bool gateup_gathers(const moe_shape& s) { return !gateup_wide(s); }
 
 // The down GEMM runs on wide pairs exactly when gate/up does, sharing its tiling and tile-unit
 // prefix; its tall tiles need an even number of scheduled m-tiles whenever gate/up has tall
@@ -230,10 +260,12 @@ void geometry_gateup(const moe_shape& s, TcParams& p) {
   p.cg = 2;
   p.wide = gateup_wide(s) ? 1 : 0;
   p.bn = bn;
+  p.gather = gateup_gathers(s) ? 1 : 0;
   TcProblem& P = p.prob[0];
   P.a_box_rows = 64;
   P.n_seg = s.E;
   P.K = s.d;
+  P.grows = s.T;
   set_m_tiles(P, s.F / 64, p.cg);
   P.tall_rows = gateup_tall_rows(s);
   P.a_seg_stride = 2 * s.F;
@@ -246,6 +278,7 @@ void geometry_gateup(const moe_shape& s, TcParams& p) {
     TcProblem& Q = p.prob[1];
     Q.a_box_rows = 64;
     Q.K = s.d;
+    Q.grows = s.T;
     set_m_tiles(Q, s.Fs / 64, p.cg);
     Q.a_seg_stride = 0;
     Q.a_m_stride = 64;
@@ -299,7 +332,7 @@ void geometry_down(const moe_shape& s, TcParams& p) {
 // Geometry plus operand pointers and tensor maps.
 int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const void* w_gate_up,
               const void* w_down, const moe_shared_expert* sh, char* ws, const Layout& L,
-              int sms, Plan& pl) {
+              const int* sorted, int sms, Plan& pl) {
   const int T = s.T, d = s.d, E = s.E, F = s.F, Fs = s.Fs;
   const int R = T * s.k;
   int* status = reinterpret_cast<int*>(ws + L.status);
@@ -325,13 +358,19 @@ int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const voi
   pg.prob[0].out = h;
   pg.prob[0].seg_off = offsets;
   pg.prob[0].ntp = ntp2;  // gate/up tiles the segments with its own n-tile cap
+  // gathering: routed rows x[sorted_token[r]] (the fused dispatch) through a one-row box map
+  // of x; else tiles of the permuted copy xs
+  pg.prob[0].gidx = sorted;
   if (encode_tmap_bf16(&pg.prob[0].tmA, w_gate_up, (uint64_t)E * 2 * F, (uint64_t)d, 64) != 0 ||
-      encode_tokens(pg.prob[0], xs_y, R, d) != 0)
+      (pg.gather ? encode_tmap_bf16(&pg.prob[0].tmB[0], x, (uint64_t)T, (uint64_t)d, 1)
+                 : encode_tokens(pg.prob[0], xs_y, R, d)) != 0)
     return -1;
   if (Fs > 0) {
     pg.prob[1].out = h_sh;
+    pg.prob[1].gidx = nullptr;  // the shared expert reads every token in order
     if (encode_tmap_bf16(&pg.prob[1].tmA, sh->w_gate_up, (uint64_t)2 * Fs, (uint64_t)d, 64) != 0 ||
-        encode_tokens(pg.prob[1], x, T, d) != 0)
+        (pg.gather ? encode_tmap_bf16(&pg.prob[1].tmB[0], x, (uint64_t)T, (uint64_t)d, 1)
+                   : encode_tokens(pg.prob[1], x, T, d)) != 0)
       return -1;
   }
 
@@ -414,7 +453,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   Plan pl;
   int bn = expert_bn(S);
   if (bf16) {
-    if (plan_bf16(S, x, w_router, w_gate_up, w_down, sh, ws, L, sms, pl) != 0) return MOE_ERR_CUDA;
+    if (plan_bf16(S, x, w_router, w_gate_up, w_down, sh, ws, L, sorted, sms, pl) != 0) return MOE_ERR_CUDA;
     if (pl.router.stages_a < 2 || pl.gateup.stages_a < 2 || pl.down.stages_a < 2) return MOE_ERR_UNSUPPORTED;
   }
   cudaEvent_t* ev = opts ? opts->stage_events : nullptr;
@@ -423,7 +462,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
 #define MOE_TRY(expr)                 \
   do {                                \
     err = (expr);                     \
-    if (err != cudaSuccess) return MOE_ERR_CUDA; \
+    if (err != cudaSuccess) return cuda_failed(err); \
   } while (0)
 
   if (!mark(0)) return MOE_ERR_CUDA;
@@ -440,8 +479,11 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                           bf16 ? gateup_bn(S) : 0, bf16 ? gateup_tall_rows(S) : 0,
                           bf16 ? ntp2 : nullptr, capacity, dropped, sorted, slot, stream));
   if (!mark(3)) return MOE_ERR_CUDA;
-  MOE_TRY(launch_gather(x, sorted, R, capacity == INT_MAX ? nullptr : offsets + S.E, S.d,
-                        bf16 ? 2 : 4, xs_y, stream));
+  // a gathering gate/up GEMM reads x through the permutation itself; otherwise (and for the
+  // fp32 expert FFN) the permuted copy xs is written first
+  if (!bf16 || !gateup_gathers(S))
+    MOE_TRY(launch_gather(x, sorted, R, capacity == INT_MAX ? nullptr : offsets + S.E, S.d,
+                          bf16 ? 2 : 4, xs_y, stream));
   if (!mark(4)) return MOE_ERR_CUDA;
   if (bf16) {
     MOE_TRY(launch_gemm_tc(kModeGateUp, pl.gateup, sms, stream));
@@ -490,14 +532,13 @@ int route_from_keys_impl(const moe_shape* s, const float* sel_key, const float* 
   const Layout L = layout_of(r);
   if (workspace_bytes < L.ntp + align256((size_t)(s->E + 1) * 4)) return MOE_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
-  if (launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, n_groups, topk_groups, topk_idx,
-                  topk_w, stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
-                      expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
-                      nullptr, INT_MAX, nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  cudaError_t e = launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, n_groups,
+                              topk_groups, topk_idx, topk_w, stream);
+  if (e == cudaSuccess)
+    e = launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
+                        expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
+                        nullptr, INT_MAX, nullptr, sorted_token, slot_pos, stream);
+  return e == cudaSuccess ? MOE_OK : cuda_failed(e);
 }
 
 }  // namespace
@@ -631,10 +672,28 @@ int moe_debug_gemm_tiles(const moe_shape* s, int which, int num_sms, const int* 
   return n;
 }
 
+int moe_debug_unclustered_pair(void* workspace, cudaStream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  int* status = static_cast<int*>(workspace);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), stream);
+  if (e == cudaSuccess) e = launch_pair_unclustered(status, stream);
+  return e == cudaSuccess ? MOE_OK : cuda_failed(e);
+}
+
+int moe_debug_wait_timeout(void* workspace, unsigned long long limit_ns, cudaStream_t stream) {
+  if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
+  int* status = static_cast<int*>(workspace);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), stream);
+  if (e == cudaSuccess) e = launch_wait_timeout(status, limit_ns, stream);
+  return e == cudaSuccess ? MOE_OK : cuda_failed(e);
+}
+
 int moe_layer_num_launches(const moe_shape* s) {
   if (check_shape(s, false) != MOE_OK) return -1;
-  // router, top-k, 3 dispatch kernels, gather, gate/up, down, combine
-  return 9;
+  // router, top-k, 3 dispatch kernels, [row gather], gate/up, down, combine: the row gather
+  // runs unless the gate/up GEMM gathers its token rows itself
+  return s->dtype == MOE_DTYPE_BF16 && gateup_gathers(*s) ? 8 : 9;
 }
 
 int moe_workspace_status(const void* workspace, int* status, int* detail) {
@@ -646,6 +705,8 @@ int moe_workspace_status(const void* workspace, int* status, int* detail) {
   if (detail) *detail = code;
   return MOE_OK;
 }
+
+const char* moe_last_cuda_error_name(void) { return cudaGetErrorName(t_last_cuda_error); }
 
 const char* moe_status_string(int status) {
   switch (status) {

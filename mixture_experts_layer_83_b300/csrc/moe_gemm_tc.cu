@@ -48,6 +48,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <string.h>
+
 #include <mutex>
 
 #include "moe_internal.h"
@@ -82,10 +84,17 @@ constexpr int kAccCols = 256;  // one accumulator: 128 lanes x up to 256 fp32 co
 // the producer counts.
 template <int CG, int WIDE> constexpr int producers_a() { return CG == 2 ? 2 : 1; }
 template <int CG, int WIDE> constexpr int producers_b() { return WIDE ? 4 : (CG == 2 ? 2 : 1); }
+// The gate/up GEMM gathers its token rows itself (the fused dispatch): its token producers
+// load the rows of x that the dispatch permutation names with TMA tile::gather4 (four rows
+// per instruction), so no permuted copy of x is ever written.
+template <int MODE> constexpr bool gathers() { return MODE == kModeGateUp; }
 // Warps 0..6 (0..11 for a wide pair) have fixed roles; the extra producers follow them.
 template <int WIDE> constexpr int base_warps() { return WIDE ? 12 : 7; }
-template <int CG, int WIDE> constexpr int threads_of() {
-  return 32 * (base_warps<WIDE>() + producers_a<CG, WIDE>() - 1 + producers_b<CG, WIDE>() - 1);
+template <int MODE, int CG, int WIDE> constexpr int warps_of() {
+  return base_warps<WIDE>() + producers_a<CG, WIDE>() - 1 + producers_b<CG, WIDE>() - 1;
+}
+template <int MODE, int CG, int WIDE> constexpr int threads_of() {
+  return 32 * warps_of<MODE, CG, WIDE>();
 }
 template <int CG, int WIDE> constexpr int acc_bufs() { return CG == 1 ? 2 : 1; }
 template <int CG, int WIDE> constexpr uint32_t tmem_cols() { return CG == 2 && !WIDE ? 256u : 512u; }
@@ -151,7 +160,7 @@ __device__ void drain_ring(uint64_t* full, const int* armed, int stages, int* er
 }
 
 template <int MODE, int CG, int WIDE>
-__global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>())
+__global__ void __launch_bounds__(threads_of<MODE, CG, WIDE>(), ctas_per_sm<CG, WIDE>())
     gemm_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   if constexpr (CG == 2) {
@@ -162,6 +171,8 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
       return;
     }
   }
+  // the gate/up GEMM gathers its token rows unless the host staged them in a permuted copy
+  const bool gather = gathers<MODE>() && p.gather != 0;
   constexpr int kGroups = WIDE ? 2 : 1;           // epilogue groups of four warps
   constexpr int kIssuers = WIDE ? 2 : 1;          // MMA issuing threads
   constexpr int kBufs = acc_bufs<CG, WIDE>();
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
   if (threadIdx.x == 32) {
     for (int i = 0; i < p.n_prob; ++i) {
       tma_prefetch_desc(&p.prob[i].tmA);
-      for (int b = 0; b < 5; ++b) tma_prefetch_desc(&p.prob[i].tmB[b]);
+      for (int b = 0; b < (gather ? 1 : 5); ++b) tma_prefetch_desc(&p.prob[i].tmB[b]);
     }
   }
   if (warp == 0) {
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
     tmem_relinquish<CG>();
   }
   if (n_seg0 > 0) {
-    for (int i = threadIdx.x; i <= n_seg0; i += threads_of<CG, WIDE>()) {
+    for (int i = threadIdx.x; i <= n_seg0; i += threads_of<MODE, CG, WIDE>()) {
       s_seg[i] = p.prob[0].seg_off[i];
       s_ntp[i] = p.prob[0].ntp[i];
     }
@@ -318,8 +329,14 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
     __syncwarp();
   } else if (b_pid >= 0) {
     // ---------------------------------------------------------------- token producer(s)
+    // Tiles of token rows by TMA.  The gathering GEMM (the fused dispatch) instead loads B row
+    // r of a routed tile from row sorted_token[r] of x (the shared expert's tile from row r)
+    // with tile::gather4, four rows per instruction, spread over the warp's 32 lanes; rows past
+    // the segment point past the end of x and read zeros (their columns are never stored).
+    // Either way the data lands in the 128-byte-swizzled layout the MMA descriptors expect and
+    // its bytes are counted on the pair leader's full barrier.
     const int pid = b_pid;
-    if (lane == 0) {
+    if (gather || lane == 0) {
       const uint64_t pol_x = l2_policy_evict_last();  // re-read by every weight tile
       int stage = 0;
       uint32_t phase = 0;
@@ -333,6 +350,12 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
         const NSplit ns = n_split<WIDE>(tl.ncols);
         const uint32_t bytes = static_cast<uint32_t>(tl.ncols * 128);
         const int kblocks = P.K >> 6;
+        // gathering: this CTA's rows of MMA 0 and MMA 1 (stage rows [0, rows0) and
+        // [rows0, rows0 + rows1)), their first rows in the tile, the end of the segment
+        const int rows0 = CG == 2 ? ns.n0 >> 1 : ns.n0;
+        const int rows1 = CG == 2 ? ns.n1 >> 1 : ns.n1;
+        const int g00 = tl.row0 + rank * rows0, g10 = tl.row0 + ns.n0 + rank * rows1;
+        const int end = tl.row0 + tl.valid;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (stage % kProdB != pid) {  // another producer's stage
             if (++stage == SB) {
@@ -341,17 +364,41 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
             }
             continue;
           }
-          if (!mbar_wait(&empty_b[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait)) {
+          bool freed = true;
+          if (lane == 0)
+            freed = mbar_wait(&empty_b[stage], phase ^ 1u, abort_flag, p.err, kErrProducerWait);
+          if (gather) freed = __shfl_sync(0xFFFFFFFFu, freed ? 1 : 0, 0) != 0;
+          if (!freed) {
             ok = false;
             break;
           }
           uint8_t* sB = ring_b + (size_t)stage * p.b_stage_bytes;
-          if (leader) {
+          if (leader && lane == 0) {
             mbar_arrive_expect_tx(&full_b[stage], bytes);
             ++armed[stage];
           }
           const uint32_t fb = CG == 2 ? mapa_shared(smem_u32(&full_b[stage]), 0) : 0u;
           const int kx = kb * 64;
+          if (gathers<MODE>() && gather) {
+            for (int i = lane; i < (rows0 + rows1) >> 2; i += 32) {
+              int src[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int r = 4 * i + j;
+                const int g = r < rows0 ? g00 + r : g10 + (r - rows0);
+                src[j] = g < end ? (P.gidx != nullptr ? __ldg(P.gidx + g) : g) : P.grows;
+              }
+              if constexpr (CG == 2)
+                tma_gather4_pair(sB + i * 512, &P.tmB[0], fb, kx, src, pol_x);
+              else
+                tma_gather4(sB + i * 512, &P.tmB[0], &full_b[stage], kx, src, pol_x);
+            }
+            if (++stage == SB) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           // each MMA's N token rows are split over a pair: the even CTA holds the first half,
           // the odd one the second (N is a multiple of 16, so each half is a multiple of 8);
           // a wide tile's second MMA follows the first in the stage
@@ -382,7 +429,7 @@ __global__ void __launch_bounds__(threads_of<CG, WIDE>(), ctas_per_sm<CG, WIDE>(
           }
         }
       }
-      if (!ok && leader) drain_ring(full_b, armed, SB, p.err);
+      if (!ok && leader && lane == 0) drain_ring(full_b, armed, SB, p.err);
     }
     __syncwarp();
   } else if (warp == 1 || (WIDE && warp == 7)) {
@@ -646,7 +693,7 @@ cudaError_t launch_single(const TcParams& p, int sms, size_t smem, cudaStream_t 
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if ((err = configure<MODE, 1, 0>(dev)) != cudaSuccess) return err;
-  gemm_tc_kernel<MODE, 1, 0><<<sms, threads_of<1, 0>(), smem, s>>>(p);
+  gemm_tc_kernel<MODE, 1, 0><<<sms, threads_of<MODE, 1, 0>(), smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -686,13 +733,40 @@ cudaError_t launch_pair(const TcParams& p, int sms, size_t smem, cudaStream_t s)
   const int pairs = resident_pairs(sms, smem, WIDE);
   if (pairs < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config(2 * pairs, threads_of<2, WIDE>(), smem, s, attr);
+  cudaLaunchConfig_t cfg = pair_config(2 * pairs, threads_of<MODE, 2, WIDE>(), smem, s, attr);
   err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MODE, 2, WIDE>, p);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
+__global__ void wait_timeout_kernel(int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  // nothing arrives on the barrier, so its first phase never completes
+  if (threadIdx.x == 0) mbar_wait(&bar, 0u, &abort_flag, err, kErrDiagWait, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_pair_unclustered(int* err, cudaStream_t s) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.err = err;
+  gemm_tc_kernel<kModeDown, 2, 1><<<2, threads_of<kModeDown, 2, 1>(), 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  return cudaGetLastError();
+}
 
 // Ring depths for an n-tile cap: the token ring holds a few stages (its loads hit L2), the
 // weight ring takes the rest of shared memory (its loads come from HBM).  A CTA of a pair
@@ -744,6 +818,7 @@ cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s)
     return cudaErrorInvalidConfiguration;
   // the forms this library uses: router on one CTA, gate/up on wide pairs, down on pairs
   if (mode == kModeRouter && p.cg == 1 && !p.wide) return launch_single<kModeRouter>(p, sms, smem, s);
+  if (mode != kModeGateUp && p.gather != 0) return cudaErrorInvalidConfiguration;
   if (mode == kModeGateUp && p.cg == 2 && p.wide && p.bn <= 2 * kAccCols)
     return launch_pair<kModeGateUp, 1>(p, sms, smem, s);
   if (mode == kModeGateUp && p.cg == 2 && !p.wide && p.bn <= kAccCols)

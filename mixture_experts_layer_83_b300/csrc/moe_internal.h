@@ -15,6 +15,7 @@ enum DeviceErr {
   kErrEpilogueWait = 3,
   kErrDrainWait = 4,
   kErrLaunchShape = 5,  // a CTA-pair kernel was launched without 2-CTA clusters
+  kErrDiagWait = 6,     // the diagnostic wait of moe_debug_wait_timeout ran out (its purpose)
 };
 
 // Epilogues of the tensor-core grouped GEMM.
@@ -50,6 +51,10 @@ struct TcProblem {
   int out_ld;          // output row stride in elements
   int out_row_base;    // output row of B row 0
   int out_valid_m;     // weight rows that produce output (router: E, down: d)
+  // Token rows gathered by the kernel itself (gate/up): B row r is row gidx[r] (row r when
+  // gidx is null) of the grows-row tensor that tmB[0] maps with a one-row box.
+  const int* gidx;
+  int grows;
 };
 
 struct TcParams {
@@ -61,6 +66,7 @@ struct TcParams {
   int stages_a;       // depth of the weight ring (16 KiB stages)
   int stages_b;       // depth of the token ring
   int b_stage_bytes;  // B rows one CTA holds per stage (bn, or bn / 2 for a pair) * 128 B
+  int gather;         // 1: token rows are gathered by TMA tile::gather4 (gate/up), 0: tiles
   int* err;           // device status word
 };
 
@@ -71,6 +77,12 @@ void gemm_tc_plan(int bn, int n_seg, TcParams& p);
 cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s);
 int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows);
+// Diagnostics of the device error path: the CTA-pair GEMM launched as two plain CTAs (no
+// cluster), which records kErrLaunchShape in *err and returns at once; and one CTA waiting on
+// an mbarrier that nothing completes, with a wall-clock limit of limit_ns, which records
+// kErrDiagWait in *err when the limit runs out and returns.
+cudaError_t launch_pair_unclustered(int* err, cudaStream_t s);
+cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s);
 
 // Router (moe_router.cu).
 cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int T, int d, int E,

@@ -11,6 +11,7 @@
 // fixed (MOE_NOALLOC_SCRATCH_BYTES); shapes that need more are rejected.  All calls on a
 // device share it, so calls whose work overlaps on the GPU (different streams, or different
 // host threads) race on it and must be serialised by the caller.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <stdint.h>
@@ -32,20 +33,47 @@ static __device__ __align__(256) int g_route_scratch[kScratchInts];
 
 constexpr int kMaxDevices = 64;
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, reached through the runtime (the library links no driver
+// library directly).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  });
+  return fn;
+}
+
 // Device address of g_route_scratch on the current device.  Host code only sees a stand-in
-// for the array, so the address is looked up once per device (with that device current) and
-// cached.
+// for the array, so the address is looked up with the device current and cached together with
+// the context it belongs to: a reset of the device (a new primary context loads the module
+// again, at a new address) makes the next call look it up again.
 int scratch_address(int** out) {
   static std::mutex mu;
   static int* addr[kMaxDevices] = {nullptr};
+  static CUcontext ctx_of[kMaxDevices] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return MOE_ERR_CUDA;
+  CUcontext ctx = nullptr;  // null until the runtime has made a context current
+  if (get(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> g(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == nullptr || ctx_of[dev] != ctx) {
     void* p = nullptr;
+    // the lookup makes the device's primary context current if none is
     if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return MOE_ERR_CUDA;
     addr[dev] = static_cast<int*>(p);
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return MOE_OK;

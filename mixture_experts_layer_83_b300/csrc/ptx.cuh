@@ -63,16 +63,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (after recording
-// `code` in *err and raising *abort) if the limit expires or another role aborted.
+// `code` in *err and raising *abort) if `limit_ns` expires or another role aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          int* err, int code) {
+                                          int* err, int code, uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicCAS(err, 0, code);
       *abort = 1;
       return false;
@@ -179,6 +179,32 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// Four rows (y[0..3], any order, out-of-range rows read the fill value) of 64 columns from x,
+// through a tensor map whose box is one row high, into four consecutive 128-byte rows of
+// shared memory; the bytes are counted on `bar`.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, const int (&y)[4], uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y[0]), "r"(y[1]),
+      "r"(y[2]), "r"(y[3]), "l"(policy)
+      : "memory");
+}
+
+// The same gather issued by either CTA of a pair, counted on the barrier at `bar_cluster`.
+__device__ __forceinline__ void tma_gather4_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, const int (&y)[4],
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y[0]), "r"(y[1]),
+      "r"(y[2]), "r"(y[3]), "l"(policy)
       : "memory");
 }
 

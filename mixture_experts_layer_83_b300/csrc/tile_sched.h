@@ -12,12 +12,18 @@
 
 namespace moe {
 
-// Tile units of a segment of n rows with n-tile cap bn: a segment of 1..tall_rows rows is one
-// unit (a tall tile per two scheduled m-tiles); otherwise each of its ceil(n / bn) n-tiles is
-// one unit per scheduled m-tile, counted twice when tall tiles exist so that a unit is always
-// worth (m_tiles / 2) tiles.
+// Whether every tile of a grouped operand set is tall: the n-tile cap is the tall-tile limit,
+// so a segment of n rows runs as ceil(n / tall_rows) tall n-tiles.
+MOE_HD bool all_tall(int bn, int tall_rows) { return tall_rows > 0 && bn <= tall_rows; }
+
+// Tile units of a segment of n rows with n-tile cap bn: when every tile is tall, one unit per
+// tall n-tile; otherwise a segment of 1..tall_rows rows is one unit (a tall tile per two
+// scheduled m-tiles) and each of the ceil(n / bn) n-tiles of a longer segment is one unit per
+// scheduled m-tile, counted twice when tall tiles exist so that a unit is always worth
+// (m_tiles / 2) tiles.
 MOE_HD int seg_units(int n, int bn, int tall_rows) {
   if (n <= 0) return 0;
+  if (all_tall(bn, tall_rows)) return (n + tall_rows - 1) / tall_rows;
   if (tall_rows > 0 && n <= tall_rows) return 1;
   return (tall_rows > 0 ? 2 : 1) * ((n + bn - 1) / bn);
 }
@@ -70,6 +76,30 @@ MOE_HD void decode_tile(const TcParams& p, const int* seg_off, const int* ntp, i
     local -= ntp[seg] * tpu;
     seg_row0 = seg_off[seg];
     seg_rows = seg_off[seg + 1] - seg_row0;
+    if (all_tall(p.bn, P.tall_rows)) {
+      // tall n-tiles: order (group of m-tile pairs, m-tile pair, n-tile), rows split evenly
+      const int pairs = P.m_tiles >> 1;
+      const int G2 = (P.group >> 1) > 0 && pairs % (P.group >> 1) == 0 ? (P.group >> 1) : 1;
+      const int ntt = units;
+      const int mg = local / (G2 * ntt);
+      const int r = local - mg * G2 * ntt;
+      const int mi = r / ntt;
+      const int j = r - mi * ntt;
+      tl.prob = prob;
+      tl.seg = seg;
+      tl.m = mg * G2 + mi;
+      tl.tall = 1;
+      tl.nt = ntt;
+      const int u16 = (seg_rows + 15) >> 4;
+      const int q16 = u16 / ntt, rem = u16 - q16 * ntt;
+      const int u0 = j * q16 + (j < rem ? j : rem);
+      const int nu = q16 + (j < rem ? 1 : 0);
+      tl.row0 = seg_row0 + u0 * 16;
+      tl.ncols = nu * 16;
+      const int left = seg_rows - u0 * 16;
+      tl.valid = left < tl.ncols ? left : tl.ncols;
+      return;
+    }
     if (P.tall_rows > 0 && units == 1) {
       tl.prob = prob;
       tl.seg = seg;

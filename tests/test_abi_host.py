@@ -105,7 +105,11 @@ def test_route_from_keys_argument_checks():
 def test_status_strings_and_launch_count():
     assert moe.moe_status_string(0) == "ok"
     assert "workspace" in moe.moe_status_string(moe.MOE_ERR_WORKSPACE)
-    assert moe.moe_layer_num_launches(shape()) == 9
+    # decode-sized segments: the gate/up GEMM gathers its token rows (no gather launch); long
+    # segments and the fp32 layer run the separate row gather
+    assert moe.moe_layer_num_launches(shape()) == 8
+    assert moe.moe_layer_num_launches(shape(T=4096)) == 9
+    assert moe.moe_layer_num_launches(shape(dtype=moe.MOE_DTYPE_F32)) == 9
     assert moe.moe_layer_num_launches(shape(T=0)) == -1
 
 
@@ -114,9 +118,10 @@ def _check_schedule(s, which, counts):
     tiles, geo = moe.moe_debug_gemm_tiles(s, which, counts)
     assert 2 <= geo["stages_a"] <= 12 and 2 <= geo["stages_b"] <= 8
     assert geo["cg"] == (1 if which == 0 else 2)
-    # one-CTA and wide-pair GEMMs may use the 227 KiB opt-in; narrow pair CTAs share their SM
-    # with a second one
-    assert geo["smem_bytes"] <= (232448 if which == 0 or geo["bn"] > 256 else 114688)
+    # one-CTA and wide-pair GEMMs may use the 227 KiB opt-in; narrow pair CTAs (experts
+    # averaging at most 64 rows) share their SM with a second one
+    narrow = which > 0 and -(-s.T * s.k // s.E) <= 64
+    assert geo["smem_bytes"] <= (114688 if narrow else 232448)
     bn = geo["bn"]
     # the expert GEMMs run on wide CTA pairs for long segments (n-tiles up to 384 token rows),
     # the router up to 256
@@ -170,9 +175,11 @@ def _check_schedule(s, which, counts):
 
 
 @pytest.mark.parametrize("which", [1, 2])
-@pytest.mark.parametrize("case", ["uniform", "ragged", "one_hot", "decode", "shared"])
+@pytest.mark.parametrize("case", ["uniform", "ragged", "one_hot", "decode", "shared", "long",
+                                  "long_skewed"])
 def test_expert_gemm_schedule_covers_every_row_once(which, case):
-    rng = np.random.default_rng(["uniform", "ragged", "one_hot", "decode", "shared"].index(case) * 10 + which)
+    rng = np.random.default_rng(["uniform", "ragged", "one_hot", "decode", "shared", "long",
+                                 "long_skewed"].index(case) * 10 + which)
     if case == "uniform":
         s = shape(T=512, d=256, E=16, k=4, F=192)
         counts = np.full(16, 512 * 4 // 16)
@@ -188,10 +195,44 @@ def test_expert_gemm_schedule_covers_every_row_once(which, case):
     elif case == "decode":
         s = shape(T=128, d=7168, E=256, k=8, F=2048, Fs=2048)
         counts = rng.multinomial(128 * 8, np.ones(256) / 256)
+    elif case == "long":    # experts average 512 rows: every tile tall
+        s = shape(T=2048, d=256, E=8, k=2, F=256)
+        counts = rng.multinomial(2048 * 2, np.ones(8) / 8)
+    elif case == "long_skewed":
+        s = shape(T=3000, d=512, E=16, k=2, F=128, Fs=64)
+        w = 1.0 / np.arange(1, 17) ** 1.2
+        counts = rng.multinomial(3000 * 2, w / w.sum())
+        counts[9] = 0
     else:
         s = shape(T=333, d=192, E=5, k=2, F=64, Fs=128)
         counts = rng.multinomial(333 * 2, np.ones(5) / 5)
     _check_schedule(s, which, counts)
+
+
+@pytest.mark.parametrize("which", [1, 2])
+def test_long_segments_run_as_tall_tiles(which):
+    """Experts averaging 384 rows or more: every segment runs as ceil(rows / 256) tall n-tiles
+    (two scheduled weight tiles, i.e. four 128-row CTA tiles, over the same token rows), rows
+    split evenly in 16-row units."""
+    s = shape(T=2048, d=256, E=8, k=2, F=256)
+    counts = np.array([700, 256, 257, 0, 1, 1000, 900, 981])
+    tiles, geo = moe.moe_debug_gemm_tiles(s, which, counts)
+    assert geo["bn"] == 256
+    m_cta = geo["m_tiles0"]
+    off = np.concatenate([[0], np.cumsum(counts)])
+    for e, n in enumerate(counts):
+        t = tiles[(tiles[:, 0] == 0) & (tiles[:, 1] == e)]
+        if n == 0:
+            assert len(t) == 0
+            continue
+        nt = -(-n // 256)
+        starts = sorted(set(t[:, 3].tolist()))
+        assert len(starts) == nt and starts[0] == off[e]
+        units = -(-n // 16)
+        sizes = [16 * (units // nt + (j < units % nt)) for j in range(nt)]
+        assert sorted(set(t[:, 4].tolist())) == sorted(set(sizes))
+        for r0 in starts:   # each n-tile meets every 128-row weight tile once
+            assert sorted(t[t[:, 3] == r0][:, 2].tolist()) == list(range(m_cta))
 
 
 @pytest.mark.parametrize("T,E", [(1, 8), (37, 8), (300, 100), (8192, 256), (128, 256), (64, 1)])
@@ -252,3 +293,13 @@ def test_group_limited_routing_arguments_are_checked_before_launch():
     s2 = shape(T=16, E=64, k=9)
     assert moe.moe_route_from_keys_grouped(s2, 16, 16, 8, 1, *args[:6], 16, 1 << 30, stream=0,
                                            check=False) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_error_path_diagnostics_check_arguments_before_launching():
+    """The two device error-path diagnostics reject a null or misaligned workspace and a wait
+    limit outside 1 us .. 1 s on the host, before anything is enqueued."""
+    assert moe.moe_debug_unclustered_pair(None, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_debug_unclustered_pair(20, stream=0, check=False) == moe.MOE_ERR_INVALID_ARG
+    for ws, limit in ((None, 10_000), (20, 10_000), (256, 999), (256, 1_000_000_001)):
+        assert moe.moe_debug_wait_timeout(ws, limit, stream=0, check=False) == \
+            moe.MOE_ERR_INVALID_ARG
