@@ -516,16 +516,20 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=int, default=None, help="override tokens (profiling cases)")
     ap.add_argument("--E", type=int, default=None, help="override routed experts (profiling)")
+    ap.add_argument("--F", type=int, default=None,
+                    help="override the expert inner width (profiling: smaller weights)")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up + timed steps of the main workload (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     c = dict(configs.CONFIGS[args.config])
-    if args.T is not None or args.E is not None:
+    if args.T is not None or args.E is not None or args.F is not None:
         c["T"] = args.T or c["T"]
         c["E"] = args.E or c["E"]
-        c["name"] = f"{c['name']} (T={c['T']}, E={c['E']} profiling case)"
+        c["F"] = args.F or c["F"]
+        c["Fs"] = min(c["Fs"], c["F"])
+        c["name"] = f"{c['name']} (T={c['T']}, E={c['E']}, F={c['F']} profiling case)"
     if args.profile:
         return run_profile(args, c)
     if args.impl == "reference":

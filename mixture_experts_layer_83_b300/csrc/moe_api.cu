@@ -36,8 +36,20 @@ int cuda_failed(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
+// The status block: the device status word, then the fused router's per-block arrival
+// counters; cleared at the start of every forward pass.
+constexpr size_t kStatusBytes = 2048;
+constexpr int kCounterInts = 256;
+constexpr size_t kCounterOffset = 512;
+// Rows of partial logits the fused router may write when it splits the reduction over d.
+constexpr int kRouterPartialRows = 2048;
+
+// Whether a layer runs the fused router (tensor-core gate GEMM with the top-k in its epilogue).
+bool fused_router(const moe_shape& s) { return s.dtype == MOE_DTYPE_BF16 && s.E <= 256; }
+
 struct Layout {
-  size_t status, logits, topk_idx, topk_w, chunk, offsets, ntp, ntp2, sorted, slot, xs_y, h, h_sh, total;
+  size_t status, logits, partial, topk_idx, topk_w, chunk, offsets, ntp, ntp2, sorted, slot, xs_y,
+      h, h_sh, total;
 };
 
 // Workspace carve-up.  xs (gathered rows) and y (expert outputs, routed rows then the shared
@@ -54,8 +66,9 @@ Layout layout_of(const moe_shape& s) {
     o += align256(bytes);
     return at;
   };
-  w.status = take(256);
-  w.logits = take((size_t)s.T * s.E * 4);
+  w.status = take(kStatusBytes);
+  w.logits = take(fused_router(s) ? 0 : (size_t)s.T * s.E * 4);
+  w.partial = take(fused_router(s) ? (size_t)kRouterPartialRows * s.E * 4 : 0);
   w.topk_idx = take(R * 4);
   w.topk_w = take(R * 4);
   w.chunk = take(nch * s.E * 4);
@@ -343,13 +356,14 @@ int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const voi
   void* h = ws + L.h;
   void* h_sh = ws + L.h_sh;
 
-  TcParams& pr = pl.router;
+  TcParams& pr = pl.router;  // the router GEMM of layers without the fused router
   geometry_router(s, sms, pr);
   pr.err = status;
   pr.prob[0].out = ws + L.logits;
-  if (encode_tmap_bf16(&pr.prob[0].tmA, w_router, (uint64_t)E, (uint64_t)d,
-                       (uint32_t)pr.prob[0].a_box_rows) != 0 ||
-      encode_tokens(pr.prob[0], x, T, d) != 0)
+  if (!fused_router(s) &&
+      (encode_tmap_bf16(&pr.prob[0].tmA, w_router, (uint64_t)E, (uint64_t)d,
+                        (uint32_t)pr.prob[0].a_box_rows) != 0 ||
+       encode_tokens(pr.prob[0], x, T, d) != 0))
     return -1;
 
   TcParams& pg = pl.gateup;
@@ -451,10 +465,29 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   void* xs_y = ws + L.xs_y;
 
   Plan pl;
+  RouterParams rp;
+  const bool fused = fused_router(S);
   int bn = expert_bn(S);
   if (bf16) {
     if (plan_bf16(S, x, w_router, w_gate_up, w_down, sh, ws, L, sorted, sms, pl) != 0) return MOE_ERR_CUDA;
-    if (pl.router.stages_a < 2 || pl.gateup.stages_a < 2 || pl.down.stages_a < 2) return MOE_ERR_UNSUPPORTED;
+    if ((!fused && pl.router.stages_a < 2) || pl.gateup.stages_a < 2 || pl.down.stages_a < 2)
+      return MOE_ERR_UNSUPPORTED;
+  }
+  if (fused) {
+    memset(&rp, 0, sizeof(rp));
+    if (router_tc_plan(S.T, S.d, S.E, sms, kRouterPartialRows, rp) != 0) return MOE_ERR_UNSUPPORTED;
+    if (encode_tmap_bf16(&rp.tmA, w_router, (uint64_t)S.E, (uint64_t)S.d, 128) != 0 ||
+        encode_tmap_bf16(&rp.tmB, x, (uint64_t)S.T, (uint64_t)S.d, (uint32_t)(rp.N / 2)) != 0)
+      return MOE_ERR_CUDA;
+    rp.bias = bias;
+    rp.topk_idx = tidx;
+    rp.topk_w = tw;
+    rp.partial = reinterpret_cast<float*>(ws + L.partial);
+    rp.counters = status + kCounterOffset / sizeof(int);
+    rp.err = status;
+    rp.k = S.k;
+    rp.G = n_groups;
+    rp.M = topk_groups;
   }
   cudaEvent_t* ev = opts ? opts->stage_events : nullptr;
   auto mark = [&](int i) -> bool { return ev == nullptr || cudaEventRecord(ev[i], stream) == cudaSuccess; };
@@ -466,15 +499,22 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   } while (0)
 
   if (!mark(0)) return MOE_ERR_CUDA;
-  MOE_TRY(cudaMemsetAsync(status, 0, sizeof(int), stream));
-  if (bf16) MOE_TRY(launch_gemm_tc(kModeRouter, pl.router, sms, stream));
-  else MOE_TRY(launch_router_logits_f32(static_cast<const float*>(x), static_cast<const float*>(w_router),
-                                        S.T, S.d, S.E, logits, stream));
-  if (!mark(1)) return MOE_ERR_CUDA;
-  MOE_TRY(launch_topk(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, logits, nullptr, bias, S.T, S.E, S.k,
-                      n_groups, topk_groups,
-                      tidx, tw, stream));
-  if (!mark(2)) return MOE_ERR_CUDA;
+  // the status word, and the fused router's arrival counters
+  MOE_TRY(cudaMemsetAsync(status, 0, fused ? kCounterOffset + kCounterInts * sizeof(int) : sizeof(int),
+                          stream));
+  if (fused) {
+    // gate GEMM, score, top-k and renormalisation in one kernel: no logits in HBM
+    MOE_TRY(launch_router_tc(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, rp, stream));
+    if (!mark(1) || !mark(2)) return MOE_ERR_CUDA;
+  } else {
+    if (bf16) MOE_TRY(launch_gemm_tc(kModeRouter, pl.router, sms, stream));
+    else MOE_TRY(launch_router_logits_f32(static_cast<const float*>(x), static_cast<const float*>(w_router),
+                                          S.T, S.d, S.E, logits, stream));
+    if (!mark(1)) return MOE_ERR_CUDA;
+    MOE_TRY(launch_topk(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, logits, nullptr, bias, S.T, S.E, S.k,
+                        n_groups, topk_groups, tidx, tw, stream));
+    if (!mark(2)) return MOE_ERR_CUDA;
+  }
   MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp,
                           bf16 ? gateup_bn(S) : 0, bf16 ? gateup_tall_rows(S) : 0,
                           bf16 ? ntp2 : nullptr, capacity, dropped, sorted, slot, stream));
@@ -528,7 +568,7 @@ int route_from_keys_impl(const moe_shape* s, const float* sel_key, const float* 
   r.d = 64;
   r.F = 64;
   r.Fs = 0;
-  r.dtype = MOE_DTYPE_BF16;
+  r.dtype = MOE_DTYPE_F32;
   const Layout L = layout_of(r);
   if (workspace_bytes < L.ntp + align256((size_t)(s->E + 1) * 4)) return MOE_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
@@ -691,9 +731,11 @@ int moe_debug_wait_timeout(void* workspace, unsigned long long limit_ns, cudaStr
 
 int moe_layer_num_launches(const moe_shape* s) {
   if (check_shape(s, false) != MOE_OK) return -1;
-  // router, top-k, 3 dispatch kernels, [row gather], gate/up, down, combine: the row gather
-  // runs unless the gate/up GEMM gathers its token rows itself
-  return s->dtype == MOE_DTYPE_BF16 && gateup_gathers(*s) ? 8 : 9;
+  // router (fused with the top-k on bf16 layers of up to 256 experts, else a GEMM and a top-k
+  // kernel), 3 dispatch kernels, [row gather], gate/up, down, combine: the row gather runs
+  // unless the gate/up GEMM gathers its token rows itself
+  const bool bf16 = s->dtype == MOE_DTYPE_BF16;
+  return (fused_router(*s) ? 1 : 2) + 3 + (bf16 && gateup_gathers(*s) ? 0 : 1) + 3;
 }
 
 int moe_workspace_status(const void* workspace, int* status, int* detail) {

@@ -84,6 +84,29 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 cudaError_t launch_pair_unclustered(int* err, cudaStream_t s);
 cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s);
 
+// Fused router of bf16 layers with E <= 256 (moe_router_tc.cu): gate GEMM on CTA pairs, score,
+// top-k and renormalisation in its epilogue.
+struct RouterParams {
+  CUtensorMap tmA;  // w_router [E][d]: box 64 columns x 128 rows
+  CUtensorMap tmB;  // x [T][d]: box 64 columns x N / 2 rows
+  const float* bias;
+  int* topk_idx;
+  float* topk_w;
+  float* partial;   // split reduction: [splits][T][E] fp32 partial logits
+  int* counters;    // split reduction: [blocks] arrivals, zero when the kernel starts
+  int* err;         // device status word
+  int T, E, k, G, M, d;
+  int N;            // tokens per block: multiple of 16, at most 256
+  int blocks, splits, kb_per_split, kblocks;
+  int stages, b_stage_bytes;
+};
+// Geometry for T tokens (-1: the shape does not fit this router).  max_partial_rows bounds
+// splits * T.
+int router_tc_plan(int T, int d, int E, int sms, int max_partial_rows, RouterParams& p);
+size_t router_tc_smem_bytes(const RouterParams& p);
+// score_fn: 0 softmax, 1 sigmoid.
+cudaError_t launch_router_tc(int score_fn, const RouterParams& p, cudaStream_t s);
+
 // Router (moe_router.cu).
 cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int T, int d, int E,
                                      float* logits, cudaStream_t s);

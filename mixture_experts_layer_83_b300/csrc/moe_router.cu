@@ -9,11 +9,10 @@
 #include <math.h>
 
 #include "moe_internal.h"
+#include "route_select.cuh"
 
 namespace moe {
 namespace {
-
-constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __global__ void router_logits_f32_kernel(const float* __restrict__ x, const float* __restrict__ wr,
                                          int T, int d, int E, float* __restrict__ logits) {
@@ -29,24 +28,8 @@ __global__ void router_logits_f32_kernel(const float* __restrict__ x, const floa
   }
 }
 
-// Does (ka, ea) precede (kb, eb) in the selection order: larger key first, then lower id.
-__device__ __forceinline__ bool before(float ka, int ea, float kb, int eb) {
-  return ka > kb || (ka == kb && ea < eb);
-}
-
-// One warp per token.  Lane l holds experts l, l+32, ... (NV slots).  k rounds: every lane
-// proposes its best untaken expert, a butterfly of shuffles agrees on the warp's best, the
-// owning lane marks it taken and lane r keeps round r's winner.  A NaN key is treated as
-// -inf, so the chosen ids are always distinct and in range.
-//   SRC 0: a = logits, softmax weights over the chosen logits.
-//   SRC 1: a = logits, key = sigmoid(logit), weights = renormalised sigmoids.
-//   SRC 2: a = supplied keys, b = supplied scores, weights = renormalised scores.
-// The optional bias is added to the key (SRC 0/1) and never to the weights.
-// Group-limited routing (G > 0; page "Expert-Parallel MoE Inference", "Load imbalance and how
-// to fight it": node-limited routing caps how many groups of experts a token may span): the
-// experts form G contiguous groups of E / G; a group's score is its largest key; the M best
-// groups are kept (equal scores: the lower group id) and the experts of the other groups are
-// excluded before the k rounds.
+// One warp per token: the token's keys are read (lane l holds experts l, l + 32, ...) and
+// select_topk picks and renormalises its k experts (see route_select.cuh).
 template <int NV, int SRC>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
                                                    const float* __restrict__ b,
@@ -55,121 +38,28 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
                                                    float* __restrict__ topk_w) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
+  float be[NV];  // this lane's experts' selection bias
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int e = lane + 32 * v;
+    be[v] = bias != nullptr && e < E ? bias[e] : 0.f;
+  }
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
     float key[NV], val[NV];
     uint32_t taken = 0;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       const int e = lane + 32 * v;
-      float kv = -INFINITY, vv = 0.f;
-      if (e < E) {
-        const float s = a[(size_t)t * E + e];
-        if (SRC == 0) {
-          kv = s;
-          vv = s;
-        } else if (SRC == 1) {
-          vv = s;
-          kv = 1.f / (1.f + expf(-s));
-        } else {
-          kv = s;
-          vv = b[(size_t)t * E + e];
-        }
-        if (SRC != 2 && bias != nullptr) kv += bias[e];
-        if (kv != kv) kv = -INFINITY;
-      } else {
+      key[v] = -INFINITY;
+      val[v] = 0.f;
+      if (e < E)
+        select_key<SRC>(a[(size_t)t * E + e], SRC == 2 ? b[(size_t)t * E + e] : 0.f, be[v],
+                        key[v], val[v]);
+      else
         taken |= 1u << v;
-      }
-      key[v] = kv;
-      val[v] = vv;
     }
-    if (G > 0) {
-      const int gsz = E / G;
-      float my_g = -INFINITY;  // lane g holds group g's score
-      for (int g = 0; g < G; ++g) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-          const int e = lane + 32 * v;
-          if (e < E && e / gsz == g) m = fmaxf(m, key[v]);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-        if (lane == g) my_g = m;
-      }
-      uint32_t gsel = 0;
-      for (int r = 0; r < M; ++r) {
-        const bool cand = lane < G && !((gsel >> lane) & 1u);
-        float bk = cand ? my_g : -INFINITY;
-        int be = cand ? lane : INT_MAX;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ok = __shfl_xor_sync(kFull, bk, off);
-          const int oe = __shfl_xor_sync(kFull, be, off);
-          if (before(ok, oe, bk, be)) {
-            bk = ok;
-            be = oe;
-          }
-        }
-        gsel |= 1u << be;
-      }
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int e = lane + 32 * v;
-        if (e < E && !((gsel >> (e / gsz)) & 1u)) taken |= 1u << v;
-      }
-    }
-    int my_e = 0;
-    float my_val = 0.f;
-    for (int r = 0; r < k; ++r) {
-      float bk = -INFINITY;
-      int be = INT_MAX;
-#pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const int e = lane + 32 * v;
-        if (!((taken >> v) & 1u) && before(key[v], e, bk, be)) {
-          bk = key[v];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ok = __shfl_xor_sync(kFull, bk, off);
-        const int oe = __shfl_xor_sync(kFull, be, off);
-        if (before(ok, oe, bk, be)) {
-          bk = ok;
-          be = oe;
-        }
-      }
-      const int wl = be & 31, wv = be >> 5;
-      float wval = 0.f;
-#pragma unroll
-      for (int v = 0; v < NV; ++v)
-        if (v == wv) wval = val[v];
-      wval = __shfl_sync(kFull, wval, wl);
-      if (lane == wl) taken |= 1u << wv;
-      if (lane == r) {
-        my_e = be;
-        my_val = wval;
-      }
-    }
-    float s;
-    if (SRC == 0) {
-      float m = lane < k ? my_val : -INFINITY;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-      s = lane < k ? expf(my_val - m) : 0.f;
-    } else if (SRC == 1) {
-      s = lane < k ? 1.f / (1.f + expf(-my_val)) : 0.f;
-    } else {
-      s = lane < k ? my_val : 0.f;
-    }
-    float sum = s;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = my_e;
-      topk_w[(size_t)t * k + lane] = s / sum;
-    }
+    select_topk<NV, SRC>(key, val, taken, E, k, G, M, topk_idx + (size_t)t * k,
+                         topk_w + (size_t)t * k);
   }
 }
 

@@ -105,10 +105,12 @@ def test_route_from_keys_argument_checks():
 def test_status_strings_and_launch_count():
     assert moe.moe_status_string(0) == "ok"
     assert "workspace" in moe.moe_status_string(moe.MOE_ERR_WORKSPACE)
-    # decode-sized segments: the gate/up GEMM gathers its token rows (no gather launch); long
-    # segments and the fp32 layer run the separate row gather
-    assert moe.moe_layer_num_launches(shape()) == 8
-    assert moe.moe_layer_num_launches(shape(T=4096)) == 9
+    # bf16 with up to 256 experts: one fused router launch (gate GEMM + top-k); decode-sized
+    # segments: the gate/up GEMM gathers its token rows (no gather launch); long segments and
+    # the fp32 layer run the separate row gather; more than 256 experts: router GEMM + top-k
+    assert moe.moe_layer_num_launches(shape()) == 7
+    assert moe.moe_layer_num_launches(shape(T=4096)) == 8
+    assert moe.moe_layer_num_launches(shape(T=65536, E=512)) == 9
     assert moe.moe_layer_num_launches(shape(dtype=moe.MOE_DTYPE_F32)) == 9
     assert moe.moe_layer_num_launches(shape(T=0)) == -1
 
