@@ -407,9 +407,23 @@ def measure(c, args, world, rank, peaks, sampler, kind):
     ms_max = max_over_ranks(ms, world)
     counts = r.counts.cpu().numpy()
     res = {"ms": ms_max, "ms_local": ms, "stages": stages, "t0": t0, "t1": t1, "counts": counts,
-           "runner": r, "dev": dev}
+           "runner": r, "dev": dev, "kernel_clocks": kernel_clocks(r)}
     res["layer"] = layer_roofline(c, counts, ms_max, peaks)
     return res
+
+
+# Nominal dense bf16 rate of one SM per clock (2.25 PFLOP/s over 148 SMs at 1.86 GHz).
+NOMINAL_BF16_FLOP_PER_CLK_SM = 8192
+B300_SMS = 148
+
+
+def kernel_clocks(r):
+    """SM clock (MHz) and duration (ms) of the last timed pass's tensor-core kernels, as CTA 0
+    of each recorded them (bf16 layers only): the clock the kernels really ran at."""
+    if r.c["dtype"] != "bf16":
+        return None
+    kc = r.moe.moe_workspace_kernel_clocks(r.ws)
+    return {k: {"sm_mhz": round(v[0], 1), "ms": round(v[1], 4)} for k, v in kc.items() if v[0] > 0}
 
 
 def layer_roofline(c, counts, ms, peaks):
@@ -441,7 +455,7 @@ def other_configs(args, world, rank, peaks):
         res = measure(c, args, world, rank, peaks, None, c["name"])
         out[c["name"]] = {"workload": workload_config(c)["workload"], "ms_per_step": res["ms"],
                           "tokens_per_s": c["T"] * world / (res["ms"] * 1e-3),
-                          "layer": res["layer"],
+                          "layer": res["layer"], "kernel_clocks": res["kernel_clocks"],
                           "stages_ms": {n: float(v) for n, v in
                                         zip(res["runner"].moe.STAGE_NAMES, res["stages"])}}
         if c["dtype"] != "bf16":
@@ -593,6 +607,14 @@ def main():
             "sm_mhz_median": clocks.get("sm_mhz"),
             "ms_x_ghz": gu_ms * clocks["sm_mhz"] / 1e3 if clocks.get("sm_mhz") else None,
             "context_frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+    kc = main_res["kernel_clocks"] or {}
+    if "gateup_gemm" in kc:
+        # the clock the GEMM ran at (its CTA 0's SM clock counter over the global timer, last
+        # timed pass), and its tensor-pipe use per clock against the nominal per-SM rate
+        mhz = kc["gateup_gemm"]["sm_mhz"]
+        roof["sm_mhz_in_kernel"] = mhz
+        roof["tensor_util_at_kernel_clock"] = achieved * 1e12 / (
+            B300_SMS * NOMINAL_BF16_FLOP_PER_CLK_SM * mhz * 1e6)
 
     dms = dec["ms"]
     dst = dec["stages"]
@@ -603,6 +625,7 @@ def main():
     # summary keys last, so that they survive in the end of the printed line
     decode = {"workload": workload_config(dc)["workload"],
               "stages_ms": {n: float(v) for n, v in zip(names, dst)},
+              "kernel_clocks": dec["kernel_clocks"],
               "cpu_baseline": cpu_baseline_entry(args, world, rank, dc, dec["dev"]),
               "experts_touched": int((dec["counts"] > 0).sum()),
               "down_gemm_hbm_frac": d_dn_bytes / (d_dn_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -630,6 +653,7 @@ def main():
                           "streams, double-buffered, overlapping the neighbouring steps' compute"},
         "gpu_launches": int(r_launches(c) * args.steps),
         "clocks": clocks,
+        "kernel_clocks": main_res["kernel_clocks"],
         "layer": main_res["layer"],
         "stages_ms": {n: float(v) for n, v in zip(names, st)},
         "other_configs": others,

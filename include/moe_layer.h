@@ -267,6 +267,15 @@ int moe_layer_num_launches(const moe_shape* s);
  * internal wait; *detail = the raw code the kernel recorded (0 if none). */
 int moe_workspace_status(const void* workspace, int* status, int* detail);
 
+/* Clock record of the latest forward pass on a workspace, SYNCHRONOUS (cudaMemcpy), for
+ * telling a kernel's work from the clock it ran at (a board at its power limit lowers the SM
+ * clock, and a sampled clock reading need not show it).  CTA 0 of each tensor-core kernel of
+ * a bf16 layer records its SM clock counter and the global timer when it starts and ends;
+ * report[2 i] = SM clock in MHz over that span, report[2 i + 1] = the span in ms, for i = 0
+ * router, 1 gate/up GEMM, 2 down GEMM (0, 0 where no record was written: the forward pass
+ * clears the records first, and fp32 layers' kernels do not record). */
+int moe_workspace_kernel_clocks(const void* workspace, double* report);
+
 /* Name of the CUDA error (e.g. "cudaErrorInvalidConfiguration") behind the latest
  * MOE_ERR_CUDA a launch returned on the calling host thread, "cudaSuccess" if none. */
 const char* moe_last_cuda_error_name(void);

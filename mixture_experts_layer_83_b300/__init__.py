@@ -30,7 +30,7 @@ EXPORTED = ("moe_layer_workspace_size", "moe_layer_forward", "moe_layer_forward_
             "moe_debug_gemm_tiles", "moe_debug_unclustered_pair", "moe_debug_wait_timeout",
             "moe_eplb_plan", "moe_load_expectation", "moe_load_report",
             "moe_layer_num_launches", "moe_workspace_status", "moe_status_string",
-            "moe_last_cuda_error_name")
+            "moe_last_cuda_error_name", "moe_workspace_kernel_clocks")
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
@@ -101,6 +101,8 @@ def lib():
         l.moe_layer_num_launches.restype = ci
         l.moe_workspace_status.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci)]
         l.moe_workspace_status.restype = ci
+        l.moe_workspace_kernel_clocks.argtypes = [vp, vp]
+        l.moe_workspace_kernel_clocks.restype = ci
         l.moe_last_cuda_error_name.argtypes = []
         l.moe_last_cuda_error_name.restype = ctypes.c_char_p
         l.moe_status_string.argtypes = [ci]
@@ -306,6 +308,18 @@ def moe_load_report(expert_counts, n_groups=1):
         raise MoeError(rc, "moe_load_report")
     return {"mean_rows_per_expert": float(rep[0]), "expert_max_over_mean": float(rep[1]),
             "group_max_over_mean": float(rep[2]), "experts_touched": int(rep[3])}
+
+
+def moe_workspace_kernel_clocks(workspace):
+    """{kernel: (SM MHz, ms)} of CTA 0 of the router, gate/up and down tensor-core kernels of
+    the latest forward pass on this workspace (synchronous)."""
+    import numpy as np
+    rep = np.zeros(6, np.float64)
+    rc = lib().moe_workspace_kernel_clocks(_ptr(workspace), rep.ctypes.data)
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_workspace_kernel_clocks")
+    return {name: (float(rep[2 * i]), float(rep[2 * i + 1]))
+            for i, name in enumerate(("router", "gateup_gemm", "down_gemm"))}
 
 
 def moe_workspace_status(workspace):

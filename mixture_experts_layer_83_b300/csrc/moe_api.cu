@@ -202,14 +202,17 @@ int gateup_bn(const moe_shape& s) {
 // separate gather).
 bool gateup_gathers(const moe_shape& s) { return !gateup_wide(s); }
 
-// The down GEMM runs on wide pairs exactly when gate/up does, sharing its tiling and tile-unit
-// prefix; its tall tiles need an even number of scheduled m-tiles whenever gate/up has tall
-// tiles, else it stays on narrow pairs (measured on the DeepSeek-V3 prefill layer: 2.19-2.25 ms
-// on wide pairs with tall tiles against 2.57-2.59 ms on narrow pairs).
+// The down GEMM runs on wide pairs exactly when gate/up does; its tall tiles need an even
+// number of scheduled m-tiles whenever gate/up has tall tiles, else it stays on narrow pairs
+// (measured on the DeepSeek-V3 prefill layer: 2.19-2.25 ms on wide pairs with tall tiles
+// against 2.57-2.59 ms on narrow pairs).
 bool down_wide(const moe_shape& s) {
   const int pairs = ((s.d + 127) / 128 + 1) / 2;
   return gateup_wide(s) && (pairs % 2 == 0 || gateup_tall_rows(s) == 0);
 }
+// (A double-buffered form, every tile two weight tiles over at most 128 rows so that two
+// accumulators fit the 512 TMEM columns, measured 3.16 ms against 2.28 ms here: 128-row MMAs
+// cannot keep the tensor pipe busy.)
 int down_bn(const moe_shape& s) { return down_wide(s) ? gateup_bn(s) : expert_bn(s); }
 int down_tall_rows(const moe_shape& s) {
   const int pairs = ((s.d + 127) / 128 + 1) / 2;
@@ -393,7 +396,7 @@ int plan_bf16(const moe_shape& s, const void* x, const void* w_router, const voi
   pd.err = status;
   pd.prob[0].out = xs_y;
   pd.prob[0].seg_off = offsets;
-  pd.prob[0].ntp = down_wide(s) ? ntp2 : ntp;
+  pd.prob[0].ntp = ntp;  // the down GEMM's own tile-unit prefix
   if (encode_tmap_bf16(&pd.prob[0].tmA, w_down, (uint64_t)E * d, (uint64_t)F, 64) != 0 ||
       encode_tokens(pd.prob[0], h, R, F) != 0)
     return -1;
@@ -499,9 +502,8 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   } while (0)
 
   if (!mark(0)) return MOE_ERR_CUDA;
-  // the status word, and the fused router's arrival counters
-  MOE_TRY(cudaMemsetAsync(status, 0, fused ? kCounterOffset + kCounterInts * sizeof(int) : sizeof(int),
-                          stream));
+  // the status word, the kernels' clock records and the fused router's arrival counters
+  MOE_TRY(cudaMemsetAsync(status, 0, kCounterOffset + kCounterInts * sizeof(int), stream));
   if (fused) {
     // gate GEMM, score, top-k and renormalisation in one kernel: no logits in HBM
     MOE_TRY(launch_router_tc(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, rp, stream));
@@ -515,7 +517,8 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                         n_groups, topk_groups, tidx, tw, stream));
     if (!mark(2)) return MOE_ERR_CUDA;
   }
-  MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bn, chunk, expert_counts, offsets, ntp,
+  MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bf16 ? down_bn(S) : bn, bf16 ? down_tall_rows(S) : 0,
+                          chunk, expert_counts, offsets, ntp,
                           bf16 ? gateup_bn(S) : 0, bf16 ? gateup_tall_rows(S) : 0,
                           bf16 ? ntp2 : nullptr, capacity, dropped, sorted, slot, stream));
   if (!mark(3)) return MOE_ERR_CUDA;
@@ -575,7 +578,7 @@ int route_from_keys_impl(const moe_shape* s, const float* sel_key, const float* 
   cudaError_t e = launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, n_groups,
                               topk_groups, topk_idx, topk_w, stream);
   if (e == cudaSuccess)
-    e = launch_dispatch(topk_idx, s->T, s->k, s->E, 256, reinterpret_cast<int*>(ws + L.chunk),
+    e = launch_dispatch(topk_idx, s->T, s->k, s->E, 256, 0, reinterpret_cast<int*>(ws + L.chunk),
                         expert_counts, expert_offsets, reinterpret_cast<int*>(ws + L.ntp), 0, 0,
                         nullptr, INT_MAX, nullptr, sorted_token, slot_pos, stream);
   return e == cudaSuccess ? MOE_OK : cuda_failed(e);
@@ -745,6 +748,21 @@ int moe_workspace_status(const void* workspace, int* status, int* detail) {
     return MOE_ERR_CUDA;
   *status = code == 0 ? MOE_OK : MOE_ERR_DEVICE;
   if (detail) *detail = code;
+  return MOE_OK;
+}
+
+int moe_workspace_kernel_clocks(const void* workspace, double* report) {
+  if (workspace == nullptr || report == nullptr) return MOE_ERR_INVALID_ARG;
+  long long r[12];
+  if (cudaMemcpy(r, static_cast<const char*>(workspace) + kClockOffset, sizeof(r),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int k = 0; k < 3; ++k) {
+    const long long dc = r[4 * k + 2] - r[4 * k], dt = r[4 * k + 3] - r[4 * k + 1];
+    const bool valid = dc > 0 && dt > 0 && dt < 100000000000ll;
+    report[2 * k] = valid ? static_cast<double>(dc) / static_cast<double>(dt) * 1e3 : 0.0;
+    report[2 * k + 1] = valid ? static_cast<double>(dt) * 1e-6 : 0.0;
+  }
   return MOE_OK;
 }
 

@@ -25,8 +25,13 @@ __device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4& v, floa
   }
 }
 
-// One warp per token; the warp stages the k (slot position, weight) pairs of its token in
-// shared memory, then each lane owns 8-column vectors lane, lane+32, ...
+// One warp per work item: a span of kChunkVec 16-byte vectors (2 KiB) of one token's output
+// row, so a short batch still spreads over many warps (each output element keeps its fixed
+// summation order, so the result does not depend on the split).  The warp stages the k (slot
+// position, weight) pairs of its token in shared memory, then each lane owns the span's
+// vectors lane, lane + 32, ...
+constexpr int kChunkVec = 128;
+
 __global__ void __launch_bounds__(256) combine_bf16_kernel(
     const uint4* __restrict__ y, const int* __restrict__ slot_pos, const float* __restrict__ w,
     int T, int k, int nvec, int R, int has_shared, uint4* __restrict__ out) {
@@ -34,13 +39,18 @@ __global__ void __launch_bounds__(256) combine_bf16_kernel(
   __shared__ float s_w[8][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
-  for (int t = blockIdx.x * wpb + warp; t < T; t += gridDim.x * wpb) {
+  const int chunks = (nvec + kChunkVec - 1) / kChunkVec;
+  const long long items = (long long)T * chunks;
+  for (long long it = (long long)blockIdx.x * wpb + warp; it < items; it += (long long)gridDim.x * wpb) {
+    const int t = static_cast<int>(it / chunks);
+    const int c = static_cast<int>(it - (long long)t * chunks);
     if (lane < k) {
       s_pos[warp][lane] = slot_pos[(size_t)t * k + lane];
       s_w[warp][lane] = w[(size_t)t * k + lane];
     }
     __syncwarp();
-    for (int v = lane; v < nvec; v += 32) {
+    const int v_end = min(nvec, (c + 1) * kChunkVec);
+    for (int v = c * kChunkVec + lane; v < v_end; v += 32) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < k; ++j)
         if (s_pos[warp][j] >= 0)  // an assignment dropped at capacity contributes nothing
@@ -87,13 +97,16 @@ cudaError_t launch_combine(const void* y, const int* slot_pos, const float* topk
   const int threads = 256, wpb = threads / 32;
   int blocks = (T + wpb - 1) / wpb;
   if (blocks > 148 * 32) blocks = 148 * 32;
-  if (bf16)
-    combine_bf16_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(y), slot_pos, topk_w,
-                                                   T, k, d / 8, R, has_shared,
-                                                   static_cast<uint4*>(out));
-  else
+  if (bf16) {
+    const long long items = (long long)T * ((d / 8 + kChunkVec - 1) / kChunkVec);
+    const long long b16 = (items + wpb - 1) / wpb;
+    combine_bf16_kernel<<<(int)(b16 < 148 * 32 ? b16 : 148 * 32), threads, 0, s>>>(
+        static_cast<const uint4*>(y), slot_pos, topk_w, T, k, d / 8, R, has_shared,
+        static_cast<uint4*>(out));
+  } else {
     combine_f32_kernel<<<blocks, threads, 0, s>>>(static_cast<const float*>(y), slot_pos, topk_w,
                                                   T, k, d, R, has_shared, static_cast<float*>(out));
+  }
   return cudaGetLastError();
 }
 

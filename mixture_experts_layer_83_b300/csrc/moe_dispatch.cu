@@ -63,10 +63,10 @@ __device__ int block_inclusive_scan(int v, int* scratch) {
 }
 
 // ntp / ntp2: prefixes of the tile units per expert (seg_units) for n-tile caps bn / bn2 and
-// tall-tile limits 0 / tall2 (the two grouped GEMMs tile the token rows differently); either
-// may be null.
+// tall-tile limits tall / tall2 (the two grouped GEMMs may tile the token rows differently);
+// either may be null.
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ chunk_counts,
-                                                             int nchunks, int E, int bn,
+                                                             int nchunks, int E, int bn, int tall,
                                                              int* __restrict__ expert_counts,
                                                              int* __restrict__ offsets,
                                                              int* __restrict__ ntp, int bn2,
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ c
   }
   const int routed = tot;
   tot = tot < capacity ? tot : capacity;  // dispatched assignments
-  const int nt = seg_units(tot, bn, 0);
+  const int nt = seg_units(tot, bn, tall);
   const int nt2 = bn2 > 0 ? seg_units(tot, bn2, tall2) : 0;
   const int inc_rows = block_inclusive_scan(tot, scratch);
   const int inc_nt = block_inclusive_scan(nt, scratch);
@@ -196,8 +196,9 @@ __global__ void gather_rows_w4_kernel(const uint32_t* __restrict__ x, const int*
 
 }  // namespace
 
-cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
-                            int* expert_counts, int* offsets, int* ntp, int bn2, int tall2,
+cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int tall,
+                            int* chunk_counts, int* expert_counts, int* offsets, int* ntp, int bn2,
+                            int tall2,
                             int* ntp2, int capacity, int* dropped, int* sorted_token,
                             int* slot_pos, cudaStream_t s) {
   const int R = T * k;
@@ -205,7 +206,7 @@ cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, in
   dispatch_count_kernel<<<nchunks, 256, E * sizeof(int), s>>>(topk_idx, R, E, chunk_counts);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, bn, expert_counts, offsets, ntp,
+  dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, bn, tall, expert_counts, offsets, ntp,
                                           bn2, tall2, ntp2, capacity, dropped);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

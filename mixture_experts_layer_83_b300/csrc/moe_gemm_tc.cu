@@ -171,6 +171,8 @@ __global__ void __launch_bounds__(threads_of<MODE, CG, WIDE>(), ctas_per_sm<CG, 
       return;
     }
   }
+  const long long clk0 = clock64();
+  const long long ns0 = static_cast<long long>(globaltimer_ns());
   // the gate/up GEMM gathers its token rows unless the host staged them in a permuted copy
   const bool gather = gathers<MODE>() && p.gather != 0;
   constexpr int kGroups = WIDE ? 2 : 1;           // epilogue groups of four warps
@@ -647,6 +649,7 @@ __global__ void __launch_bounds__(threads_of<MODE, CG, WIDE>(), ctas_per_sm<CG, 
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, tmem_cols<CG, WIDE>());
   }
+  if (blockIdx.x == 0 && threadIdx.x == 0) record_clocks(p.err, MODE, clk0, ns0);
 }
 
 size_t fixed_smem_bytes(int n_seg, int wide) {

@@ -21,6 +21,20 @@ enum DeviceErr {
 // Epilogues of the tensor-core grouped GEMM.
 enum GemmMode { kModeRouter = 0, kModeGateUp = 1, kModeDown = 2 };
 
+// Clock records in the status block: CTA 0 of each tensor-core kernel writes {clock64 at start,
+// %globaltimer at start, clock64 at end, %globaltimer at end} to slot (router 0, gate/up 1,
+// down 2), 64 bit each, starting kClockOffset bytes after the status word.
+constexpr int kClockOffset = 64;
+__device__ __forceinline__ void record_clocks(int* status, int slot, long long c0, long long t0) {
+  long long t1;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+  long long* r = reinterpret_cast<long long*>(reinterpret_cast<char*>(status) + kClockOffset) + 4 * slot;
+  r[0] = c0;
+  r[1] = t0;
+  r[2] = clock64();
+  r[3] = t1;
+}
+
 // Assignments handled per block by the dispatch histogram / permutation kernels.
 constexpr int kDispatchChunk = 1024;
 constexpr int kDispatchWarps = 8;
@@ -117,11 +131,12 @@ cudaError_t launch_topk(int src, const float* a, const float* b, const float* bi
 
 // Dispatch (moe_dispatch.cu).
 // ntp / ntp2 (either may be null): per-expert prefixes of tile units (seg_units) for n-tile
-// caps bn / bn2 and tall-tile limits 0 / tall2.
+// caps bn / bn2 and tall-tile limits tall / tall2.
 // capacity: per-expert limit of dispatched assignments (INT_MAX: dropless); *dropped (may be
 // null) receives the number dropped; a dropped assignment gets slot_pos -1.
-cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int* chunk_counts,
-                            int* expert_counts, int* offsets, int* ntp, int bn2, int tall2,
+cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, int tall,
+                            int* chunk_counts, int* expert_counts, int* offsets, int* ntp, int bn2,
+                            int tall2,
                             int* ntp2, int capacity, int* dropped, int* sorted_token,
                             int* slot_pos, cudaStream_t s);
 // rows_dev (may be null): device row count replacing R (rows dispatched under a capacity).

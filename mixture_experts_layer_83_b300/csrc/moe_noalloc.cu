@@ -106,7 +106,7 @@ extern "C" int moe_route_from_keys_noalloc(const moe_shape* s, const float* sel_
   if (launch_topk(2, sel_key, gate_score, nullptr, s->T, s->E, s->k, 0, 0, topk_idx, topk_w, stream) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, scratch, expert_counts, expert_offsets,
+  if (launch_dispatch(topk_idx, s->T, s->k, s->E, 256, 0, scratch, expert_counts, expert_offsets,
                       nullptr, 0, 0, nullptr, INT_MAX, nullptr, sorted_token, slot_pos, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
     if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrLaunchShape);
     return;
   }
+  const long long clk0 = clock64();
+  const long long ns0 = static_cast<long long>(globaltimer_ns());
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc<2>(tmem_base, 256);
   }
+  if (blockIdx.x == 0 && threadIdx.x == 0) record_clocks(p.err, 0, clk0, ns0);
 }
 
 template <int SRC, int NV>

@@ -215,3 +215,20 @@ def test_forward_dispatch_tables_match_oracle_for_gpu_routing():
     res = to_host(gpu_forward(cfg, dev))
     counts, _ = check_dispatch(cfg, res["topk_idx"], res["counts"], res["sorted_token"])
     assert counts.sum() == cfg["T"] * cfg["k"]
+
+
+def test_kernel_clock_records():
+    """After a bf16 forward pass the router, gate/up and down kernels have recorded a plausible
+    SM clock and duration; an fp32 pass (CUDA-core kernels) records none."""
+    import mixture_experts_layer_83_b300 as moe
+    c = make_shape(T=256, d=256, E=16, k=4, F=128, Fs=64, dtype="bf16", score=SIGMOID,
+                   bias_range=0.01, seed=11, name="clocks")
+    res = gpu_forward(c, moe_inputs.upload(c, moe_inputs.host_inputs(c)))
+    torch.cuda.synchronize()
+    kc = moe.moe_workspace_kernel_clocks(res["workspace"])
+    for name, (mhz, ms) in kc.items():
+        assert 300 < mhz < 2500 and 0 < ms < 100, (name, mhz, ms)
+    c32 = dict(c, dtype="f32", name="clocks-f32")
+    res = gpu_forward(c32, moe_inputs.upload(c32, moe_inputs.host_inputs(c32)))
+    torch.cuda.synchronize()
+    assert all(v == (0.0, 0.0) for v in moe.moe_workspace_kernel_clocks(res["workspace"]).values())
