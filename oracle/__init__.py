@@ -59,12 +59,15 @@ def lib():
         l.oracle_capacity.argtypes = [ci, ci, ci, ctypes.c_double]
         l.oracle_eplb_plan.argtypes = [vp, ci, ci, ci, vp, vp, vp]
         l.oracle_dispatch_capacity.argtypes = [ci, ci, ci, vp, ci, vp, vp, vp, vp, vp]
+        l.oracle_dispatch_reroute.argtypes = [ci, ci, ci, ci, vp, ci, vp, vp, vp, vp, vp, vp, vp]
+        l.oracle_served_weights.argtypes = [ci, ci, ci, vp, vp, vp]
         l.oracle_gather.argtypes = [ci, ci, vp, vp, vp]
         l.oracle_combine.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
         l.oracle_swiglu_ffn.argtypes = [ci, ci, ci, vp, vp, vp, vp]
         l.oracle_layer_rows.argtypes = [ctypes.POINTER(OracleLayer), ci, vp, vp, vp, vp]
         for f in ("oracle_router_scores", "oracle_topk", "oracle_topk_grouped", "oracle_dispatch",
-                  "oracle_capacity", "oracle_dispatch_capacity", "oracle_eplb_plan",
+                  "oracle_capacity", "oracle_dispatch_capacity", "oracle_dispatch_reroute",
+                  "oracle_served_weights", "oracle_eplb_plan",
                   "oracle_gather",
                   "oracle_combine", "oracle_swiglu_ffn", "oracle_layer_rows"):
             getattr(l, f).restype = ci
@@ -152,6 +155,33 @@ def dispatch_capacity(topk_idx, E, cap):
                                           _p(offsets), _p(st), _p(sp), _p(dropped)),
            "dispatch_capacity")
     return counts, offsets, st[:offsets[-1]], sp, int(dropped[0])
+
+
+def dispatch_reroute(cand, k, E, cap):
+    """Capacity with rerouting (see moe_oracle.c): cand [T][kc] candidates in selection order.
+    Returns (assign [T][k] expert or -1, assign_cand [T][k], counts, offsets, sorted_token,
+    slot_pos, dropped)."""
+    cand = np.ascontiguousarray(cand, dtype=np.int32)
+    T, kc = cand.shape
+    assign = np.empty((T, k), dtype=np.int32); ac = np.empty((T, k), dtype=np.int32)
+    counts = np.empty(E, dtype=np.int32); offsets = np.empty(E + 1, dtype=np.int32)
+    st = np.empty(max(T * k, 1), dtype=np.int32); sp = np.empty((T, k), dtype=np.int32)
+    dropped = np.zeros(1, dtype=np.int32)
+    _check(lib().oracle_dispatch_reroute(T, E, k, kc, _p(cand), int(cap), _p(assign), _p(ac),
+                                         _p(counts), _p(offsets), _p(st), _p(sp), _p(dropped)),
+           "dispatch_reroute")
+    return assign, ac, counts, offsets, st[:offsets[-1]], sp, int(dropped[0])
+
+
+def served_weights(score, assign):
+    """Weights renormalised over each token's serving experts (0 for dropped slots)."""
+    score = np.ascontiguousarray(score, dtype=np.float64)
+    assign = np.ascontiguousarray(assign, dtype=np.int32)
+    T, k = assign.shape
+    w = np.empty((T, k))
+    _check(lib().oracle_served_weights(T, score.shape[1], k, _p(score), _p(assign), _p(w)),
+           "served_weights")
+    return w
 
 
 def eplb_plan(load, n_gpus, n_redundant):

@@ -254,6 +254,112 @@ int oracle_dispatch_capacity(int T, int E, int k, const int* topk_idx, int capac
   return 0;
 }
 
+/* Capacity with rerouting (same page and section: overflow tokens are dropped or rerouted to
+ * their next-best expert).  The pages give no procedure; the reading taken here runs in rounds.
+ * Each token t has kc candidates cand[t][0..kc-1], its experts in selection order (its top-kc).
+ * In round 0 slot j of every token proposes candidate j (its top-k).  In a round, proposals are
+ * taken in token order (then slot order) and an expert accepts a proposal while it holds fewer
+ * than `capacity` accepted slots.  After the round, each rejected slot of a token (in slot
+ * order) takes the token's next unused candidate and proposes it in the next round; a slot
+ * with no candidate left is dropped.  Rounds continue while a slot proposes.
+ * assign[t][j] = the serving expert or -1 (dropped), assign_cand[t][j] = its candidate index or
+ * -1; counts / offsets / sorted_token / slot_pos are the dispatch tables of the final
+ * assignment (per expert, its tokens in ascending order); *dropped = dropped slots. */
+int oracle_dispatch_reroute(int T, int E, int k, int kc, const int* cand, int capacity,
+                            int* assign, int* assign_cand, int* counts, int* offsets,
+                            int* sorted_token, int* slot_pos, int* dropped) {
+  if (T < 0 || E < 1 || k < 1 || kc < k || kc > E || capacity < 0 || !cand || !assign ||
+      !counts || !offsets)
+    return -1;
+  for (size_t i = 0; i < (size_t)T * kc; ++i)
+    if (cand[i] < 0 || cand[i] >= E) return -1;
+  const size_t R = (size_t)T * k;
+  int* fill = (int*)calloc((size_t)E, sizeof(int));
+  int* prop = (int*)malloc(R * sizeof(int));    /* proposing candidate index, -1 = none */
+  int* rejected = (int*)malloc(R * sizeof(int));
+  int* next = (int*)malloc((size_t)(T > 0 ? T : 1) * sizeof(int));
+  if (!fill || !prop || !rejected || !next) {
+    free(fill); free(prop); free(rejected); free(next);
+    return -1;
+  }
+  for (int t = 0; t < T; ++t) {
+    next[t] = k;
+    for (int j = 0; j < k; ++j) {
+      prop[(size_t)t * k + j] = j;
+      assign[(size_t)t * k + j] = -1;
+      if (assign_cand) assign_cand[(size_t)t * k + j] = -1;
+    }
+  }
+  int proposing = T * k > 0;
+  while (proposing) {
+    for (size_t i = 0; i < R; ++i) rejected[i] = 0;
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j) {
+        const size_t i = (size_t)t * k + j;
+        if (prop[i] < 0) continue;
+        const int e = cand[(size_t)t * kc + prop[i]];
+        if (fill[e] < capacity) {
+          ++fill[e];
+          assign[i] = e;
+          if (assign_cand) assign_cand[i] = prop[i];
+        } else {
+          rejected[i] = 1;
+        }
+        prop[i] = -1;
+      }
+    proposing = 0;
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j) {
+        const size_t i = (size_t)t * k + j;
+        if (!rejected[i] || next[t] >= kc) continue;
+        prop[i] = next[t]++;
+        proposing = 1;
+      }
+  }
+  int ndrop = 0, p = 0;
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) {
+    int n = 0;
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j)
+        if (assign[(size_t)t * k + j] == e) {
+          if (sorted_token) sorted_token[p] = t;
+          if (slot_pos) slot_pos[(size_t)t * k + j] = p;
+          ++p;
+          ++n;
+        }
+    counts[e] = n;
+    offsets[e + 1] = offsets[e] + n;
+  }
+  for (size_t i = 0; i < R; ++i)
+    if (assign[i] < 0) {
+      if (slot_pos) slot_pos[i] = -1;
+      ++ndrop;
+    }
+  if (dropped) *dropped = ndrop;
+  free(fill); free(prop); free(rejected); free(next);
+  return 0;
+}
+
+/* Gate weights renormalised over the experts that serve each token (the renormalisation of the
+ * top-k weights with the served experts in place of the top-k): w[t][j] = score[t][assign] /
+ * sum over the token's served slots, 0 for a dropped slot. */
+int oracle_served_weights(int T, int E, int k, const double* score, const int* assign, double* w) {
+  if (T < 0 || E < 1 || k < 1 || !score || !assign || !w) return -1;
+  for (int t = 0; t < T; ++t) {
+    double den = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int e = assign[(size_t)t * k + j];
+      if (e >= 0) den += score[(size_t)t * E + e];
+    }
+    for (int j = 0; j < k; ++j) {
+      const int e = assign[(size_t)t * k + j];
+      w[(size_t)t * k + j] = e >= 0 ? score[(size_t)t * E + e] / den : 0.0;
+    }
+  }
+  return 0;
+}
+
 int oracle_gather(int R, int d, const int* sorted_token, const double* x, double* xs) {
   if (R < 0 || d < 1 || !sorted_token || !x || !xs) return -1;
   for (int p = 0; p < R; ++p)

@@ -81,6 +81,16 @@ int oracle_capacity(int T, int E, int k, double capacity_factor);
  * order are dispatched and the rest dropped.  counts [E] = dispatched per expert, offsets
  * [E+1], sorted_token [dispatched total], slot_pos [T][k] = position or -1 (dropped),
  * *dropped = dropped assignments (any output except counts / offsets may be NULL). */
+/* Capacity with rerouting of overflow to the next-best expert (rounds; see moe_oracle.c):
+ * cand [T][kc] = each token's experts in selection order (kc >= k); outputs the serving expert
+ * and candidate index of every slot (-1: dropped) and the dispatch tables of that assignment. */
+int oracle_dispatch_reroute(int T, int E, int k, int kc, const int* cand, int capacity,
+                            int* assign, int* assign_cand, int* counts, int* offsets,
+                            int* sorted_token, int* slot_pos, int* dropped);
+
+/* Weights renormalised over each token's serving experts (0 for a dropped slot). */
+int oracle_served_weights(int T, int E, int k, const double* score, const int* assign, double* w);
+
 int oracle_dispatch_capacity(int T, int E, int k, const int* topk_idx, int capacity,
                              int* counts, int* offsets, int* sorted_token, int* slot_pos,
                              int* dropped);

@@ -503,3 +503,98 @@ def test_softmax_bias_moves_selection_not_weights():
     assert idx.tolist() == [[2, 0]]
     assert w[0, 0] == pytest.approx(1 / (1 + math.exp(2)), abs=1e-15)
     assert w[0, 1] == pytest.approx(1 / (1 + math.exp(-2)), abs=1e-15)
+
+
+# ------------------------------------------------------------------ rerouting at capacity
+def test_reroute_hand_case_overflow_moves_to_next_best():
+    """4 tokens, 3 experts, top-1 with all 3 candidates, capacity 2.  Round 0: tokens 0 and 1
+    fill expert 0, token 2 overflows, token 3 takes expert 1; round 1: token 2 moves to its
+    next-best expert 1, which still has a slot."""
+    cand = [[0, 1, 2], [0, 2, 1], [0, 1, 2], [1, 0, 2]]
+    assign, ac, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, 1, 3, 2)
+    assert assign[:, 0].tolist() == [0, 0, 1, 1] and ac[:, 0].tolist() == [0, 0, 1, 0]
+    assert counts.tolist() == [2, 2, 0] and offsets.tolist() == [0, 2, 4, 4]
+    assert st.tolist() == [0, 1, 2, 3] and sp[:, 0].tolist() == [0, 1, 2, 3] and dropped == 0
+
+
+def test_reroute_hand_case_candidates_run_out():
+    """Same candidates, capacity 1.  Round 0: token 0 -> 0, token 3 -> 1, tokens 1 and 2
+    rejected; round 1: token 1 takes expert 2, token 2 finds expert 1 full; round 2: token 2
+    finds expert 2 full and has no candidate left: dropped."""
+    cand = [[0, 1, 2], [0, 2, 1], [0, 1, 2], [1, 0, 2]]
+    assign, ac, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, 1, 3, 1)
+    assert assign[:, 0].tolist() == [0, 2, -1, 1] and ac[:, 0].tolist() == [0, 1, -1, 0]
+    assert counts.tolist() == [1, 1, 1] and st.tolist() == [0, 3, 1]
+    assert sp[:, 0].tolist() == [0, 2, -1, 1] and dropped == 1
+
+
+def test_reroute_hand_case_two_slots_take_successive_candidates():
+    """Top-2 of 4 experts, capacity 1: token 0 fills experts 0 and 1; token 1's two rejected
+    slots take its next candidates in slot order (slot 0 -> expert 3, slot 1 -> expert 2)."""
+    cand = [[0, 1, 2, 3], [0, 1, 3, 2]]
+    assign, ac, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, 2, 4, 1)
+    assert assign.tolist() == [[0, 1], [3, 2]] and ac.tolist() == [[0, 1], [2, 3]]
+    assert counts.tolist() == [1, 1, 1, 1] and st.tolist() == [0, 0, 1, 1]
+    assert sp.tolist() == [[0, 1], [3, 2]] and dropped == 0
+
+
+def _skewed_candidates(rng, T, E, kc):
+    w = 1.0 / np.arange(1, E + 1) ** 1.5
+    keys = np.log(w)[None, :] + rng.standard_normal((T, E))
+    idx, _, _ = oracle.topk(keys, np.ones((T, E)), kc)
+    return idx
+
+
+@pytest.mark.parametrize("T,E,k,extra,cap", [(50, 8, 2, 2, 6), (200, 16, 4, 4, 30), (64, 8, 8, 0, 40),
+                                             (100, 12, 3, 9, 20), (30, 6, 1, 5, 3)])
+def test_reroute_invariants(T, E, k, extra, cap):
+    """Random skewed candidate lists: no expert over capacity; served + dropped = T*k; each
+    token's serving experts are distinct candidates of its own list; the tables are a stable
+    counting sort of the assignment.  Catches: double-booking an expert, a token served twice
+    by one expert, candidates taken out of order."""
+    rng = np.random.default_rng(T + E + k)
+    cand = _skewed_candidates(rng, T, E, k + extra)
+    assign, ac, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, k, E, cap)
+    assert counts.max() <= cap and counts.sum() + dropped == T * k
+    for t in range(T):
+        served = [(e, c) for e, c in zip(assign[t], ac[t]) if e >= 0]
+        assert len({e for e, _ in served}) == len(served)
+        for e, c in served:
+            assert cand[t][c] == e
+    want_st = [t for e in range(E) for t in range(T) for j in range(k) if assign[t, j] == e]
+    assert st.tolist() == want_st
+    for t in range(T):
+        for j in range(k):
+            assert (sp[t, j] < 0) == (assign[t, j] < 0)
+            if sp[t, j] >= 0:
+                assert st[sp[t, j]] == t and offsets[assign[t, j]] <= sp[t, j] < offsets[assign[t, j] + 1]
+
+
+@pytest.mark.parametrize("T,E,k,cap", [(40, 6, 2, 5), (100, 16, 4, 20), (33, 4, 3, 1)])
+def test_reroute_without_extra_candidates_is_capacity_dropping(T, E, k, cap):
+    """With no candidate beyond the top-k the procedure is the capacity dispatch that drops."""
+    rng = np.random.default_rng(7 * T + k)
+    cand = _skewed_candidates(rng, T, E, k)
+    assign, _, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, k, E, cap)
+    c2, o2, st2, sp2, d2 = oracle.dispatch_capacity(cand, E, cap)
+    assert counts.tolist() == c2.tolist() and st.tolist() == st2.tolist()
+    assert sp.tolist() == sp2.tolist() and dropped == d2
+    assert np.array_equal(assign, np.where(sp2 >= 0, cand, -1))
+
+
+def test_reroute_with_room_everywhere_is_dropless():
+    """A capacity no expert can reach: the top-k of every token, dropless tables."""
+    rng = np.random.default_rng(3)
+    cand = _skewed_candidates(rng, 80, 10, 6)
+    assign, _, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, 4, 10, 80 * 4)
+    c2, o2, st2, sp2 = oracle.dispatch(cand[:, :4], 10)
+    assert np.array_equal(assign, cand[:, :4]) and dropped == 0
+    assert counts.tolist() == c2.tolist() and st.tolist() == st2.tolist() and sp.tolist() == sp2.tolist()
+
+
+def test_served_weights_renormalise_over_serving_experts():
+    score = np.array([[0.5, 0.3, 0.2], [0.1, 0.6, 0.3]])
+    w = oracle.served_weights(score, np.array([[0, 2], [-1, -1]]))
+    np.testing.assert_allclose(w, [[0.5 / 0.7, 0.2 / 0.7], [0.0, 0.0]], rtol=0, atol=1e-15)
+    w = oracle.served_weights(score, np.array([[1, -1], [2, 1]]))
+    np.testing.assert_allclose(w, [[1.0, 0.0], [0.3 / 0.9, 0.6 / 0.9]], rtol=0, atol=1e-15)
