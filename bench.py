@@ -497,7 +497,8 @@ def skew_report(args, world, rank):
            "groups": f"{groups} contiguous groups of {c['E'] // groups} experts"}
     variants = (("dropless", {}),
                 ("group_limited_4_of_8", dict(n_groups=groups, topk_groups=4)),
-                ("capacity_1.25", dict(capacity_factor=1.25, dropped=dropped)))
+                ("capacity_1.25", dict(capacity_factor=1.25, dropped=dropped)),
+                ("capacity_1.25_reroute_4", dict(capacity_factor=1.25, dropped=dropped, reroute=4)))
     for name, opts in variants:
         r.options = opts
         ms, _, _ = r.timed(args.steps, args.warmup, world, with_stages=False)

@@ -134,9 +134,20 @@ typedef struct {
    * expert's slots in token order and an assignment beyond the capacity is dropped: it skips
    * the expert FFN and contributes nothing to its token's output (the token's other weights
    * are not renormalised; the layer output carries no residual).  expert_counts then counts
-   * the dispatched assignments.  0: dropless.  Negative, NaN or infinite: MOE_ERR_INVALID_ARG. */
-  float capacity_factor;
+   * the dispatched assignments.  0: dropless.  Negative, NaN or infinite: MOE_ERR_INVALID_ARG.
+   * A double, so that a factor written in decimal (0.8) gives the capacity of its exact value
+   * where factor * T * k / E is a whole number (a float 0.8 would round it up by one). */
+  double capacity_factor;
   int* dropped; /* NULL, or a device int (16-byte aligned) receiving the dropped assignments */
+  /* Rerouting instead of dropping (same section: overflow tokens are rerouted to their
+   * next-best expert); needs capacity_factor > 0.  reroute = the candidates each token may
+   * take beyond its top-k (its next-best experts in selection order; k + reroute <= 32 and
+   * <= E).  In round 0 every token's k slots propose its top-k; an expert accepts proposals in
+   * token order while it has room; each rejected slot takes its token's next unused candidate
+   * and proposes it in the next round; a slot whose candidates run out is dropped.  The gate
+   * weights are renormalised over the experts that serve the token.  topk_idx_out then holds
+   * the serving expert of every slot (-1: dropped) and topk_w_out those weights.  0: drop. */
+  int reroute;
 } moe_forward_opts;
 
 /* moe_layer_forward with options (stage timing events, group-limited routing); opts may be

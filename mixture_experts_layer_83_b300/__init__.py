@@ -46,8 +46,8 @@ class MoeSharedExpert(ctypes.Structure):
 
 class MoeForwardOpts(ctypes.Structure):
     _fields_ = [("stage_events", ctypes.POINTER(ctypes.c_void_p)), ("n_groups", ctypes.c_int),
-                ("topk_groups", ctypes.c_int), ("capacity_factor", ctypes.c_float),
-                ("dropped", ctypes.c_void_p)]
+                ("topk_groups", ctypes.c_int), ("capacity_factor", ctypes.c_double),
+                ("dropped", ctypes.c_void_p), ("reroute", ctypes.c_int)]
 
 
 class MoeError(RuntimeError):
@@ -159,11 +159,13 @@ def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, sha
                       out, expert_counts, workspace, workspace_bytes=None, stream=None,
                       topk_idx_out=None, topk_w_out=None, sorted_token_out=None,
                       stage_events=None, n_groups=0, topk_groups=0, capacity_factor=0.0,
-                      dropped=None, check=True):
+                      dropped=None, reroute=0, check=True):
     """One forward pass; ``shared_expert`` is None or (w_gate_up, w_down); ``n_groups`` /
     ``topk_groups`` select group-limited routing (0 / 0: plain top-k); ``capacity_factor`` > 0
     caps each expert's assignments (``dropped``: optional device int receiving the number
-    dropped).  Returns the status (raises MoeError on failure when ``check``)."""
+    dropped); ``reroute`` > 0 (with a capacity) moves overflow to each token's next-best
+    experts instead of dropping it.  Returns the status (raises MoeError on failure when
+    ``check``)."""
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     args = [ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
@@ -171,7 +173,7 @@ def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, sha
             _ptr(workspace), int(workspace_bytes), _stream(stream), _ptr(topk_idx_out),
             _ptr(topk_w_out), _ptr(sorted_token_out)]
     if stage_events is None and n_groups == 0 and topk_groups == 0 and capacity_factor == 0 \
-            and dropped is None:
+            and dropped is None and reroute == 0:
         rc = lib().moe_layer_forward(*args)
     else:
         arr = None
@@ -181,7 +183,7 @@ def moe_layer_forward(shape, x, w_router, w_gate_up, w_down, score_fn, bias, sha
                     e.record()
             arr = (ctypes.c_void_p * MOE_NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
         opts = MoeForwardOpts(arr, int(n_groups), int(topk_groups), float(capacity_factor),
-                              _ptr(dropped))
+                              _ptr(dropped), int(reroute))
         rc = lib().moe_layer_forward_ex(*args, ctypes.byref(opts))
     if check and rc != MOE_OK:
         raise MoeError(rc, "moe_layer_forward")

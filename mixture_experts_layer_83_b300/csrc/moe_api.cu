@@ -48,8 +48,8 @@ constexpr int kRouterPartialRows = 2048;
 bool fused_router(const moe_shape& s) { return s.dtype == MOE_DTYPE_BF16 && s.E <= 256; }
 
 struct Layout {
-  size_t status, logits, partial, topk_idx, topk_w, chunk, offsets, ntp, ntp2, sorted, slot, xs_y,
-      h, h_sh, total;
+  size_t status, logits, partial, topk_idx, topk_w, chunk, offsets, ntp, ntp2, sorted, slot,
+      cand, cand_val, prop, assign_c, next_c, fill, left, xs_y, h, h_sh, total;
 };
 
 // Workspace carve-up.  xs (gathered rows) and y (expert outputs, routed rows then the shared
@@ -77,6 +77,14 @@ Layout layout_of(const moe_shape& s) {
   w.ntp2 = take((size_t)(s.E + 1) * 4);
   w.sorted = take(R * 4);
   w.slot = take(R * 4);
+  // rerouting at capacity: up to 32 candidates per token and the rounds' state
+  w.cand = take((size_t)s.T * 32 * 4);
+  w.cand_val = take((size_t)s.T * 32 * 4);
+  w.prop = take(R * 4);
+  w.assign_c = take(R * 4);
+  w.next_c = take((size_t)s.T * 4);
+  w.fill = take((size_t)s.E * 4);
+  w.left = take((size_t)s.E * 4);
   w.xs_y = take((R + tsh) * s.d * elt);
   w.h = take(R * s.F * elt);
   w.h_sh = take(tsh * (size_t)s.Fs * elt);
@@ -115,10 +123,10 @@ int check_groups(const moe_shape& s, int G, int M) {
 
 // Expert capacity for a capacity factor: ceil(factor * T * k / E) dispatched assignments per
 // expert, INT_MAX for a factor of 0 (dropless).  -1: an invalid factor.
-int capacity_of(const moe_shape& s, float factor) {
-  if (factor == 0.f) return INT_MAX;
-  if (!(factor > 0.f) || !isfinite(factor)) return -1;
-  const double c = ceil((double)factor * ((double)s.T * (double)s.k / (double)s.E));
+int capacity_of(const moe_shape& s, double factor) {
+  if (factor == 0.0) return INT_MAX;
+  if (!(factor > 0.0) || !isfinite(factor)) return -1;
+  const double c = ceil(factor * ((double)s.T * (double)s.k / (double)s.E));
   return c >= (double)INT_MAX ? INT_MAX : (int)c;
 }
 
@@ -443,8 +451,14 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   const int n_groups = opts ? opts->n_groups : 0, topk_groups = opts ? opts->topk_groups : 0;
   rc = check_groups(*s, n_groups, topk_groups);
   if (rc != MOE_OK) return rc;
-  const int capacity = capacity_of(*s, opts ? opts->capacity_factor : 0.f);
+  const int capacity = capacity_of(*s, opts ? opts->capacity_factor : 0.0);
   if (capacity < 0) return MOE_ERR_INVALID_ARG;
+  // rerouting: `reroute` candidates beyond the top-k, only with a capacity
+  const int reroute = opts ? opts->reroute : 0;
+  if (reroute < 0 || (reroute > 0 && capacity == INT_MAX) || s->k + reroute > kMaxK ||
+      s->k + reroute > s->E)
+    return MOE_ERR_INVALID_ARG;
+  const int kc = reroute > 0 ? s->k + reroute : 0;
   int* dropped = opts ? opts->dropped : nullptr;
   if (dropped != nullptr && !aligned16(dropped)) return MOE_ERR_INVALID_ARG;
   const int sms = device_sm_count();
@@ -465,6 +479,11 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   int* ntp2 = reinterpret_cast<int*>(ws + L.ntp2);
   int* sorted = sorted_token_out ? sorted_token_out : reinterpret_cast<int*>(ws + L.sorted);
   int* slot = reinterpret_cast<int*>(ws + L.slot);
+  int* cand = reinterpret_cast<int*>(ws + L.cand);
+  float* cand_val = reinterpret_cast<float*>(ws + L.cand_val);
+  // the router writes candidates when rerouting, else the top-k and its weights
+  int* ridx = kc > 0 ? cand : tidx;
+  float* rw = kc > 0 ? cand_val : tw;
   void* xs_y = ws + L.xs_y;
 
   Plan pl;
@@ -483,8 +502,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
         encode_tmap_bf16(&rp.tmB, x, (uint64_t)S.T, (uint64_t)S.d, (uint32_t)(rp.N / 2)) != 0)
       return MOE_ERR_CUDA;
     rp.bias = bias;
-    rp.topk_idx = tidx;
-    rp.topk_w = tw;
+    rp.topk_idx = ridx;
+    rp.topk_w = rw;
+    rp.kc = kc;
     rp.partial = reinterpret_cast<float*>(ws + L.partial);
     rp.counters = status + kCounterOffset / sizeof(int);
     rp.err = status;
@@ -514,13 +534,20 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                                           S.T, S.d, S.E, logits, stream));
     if (!mark(1)) return MOE_ERR_CUDA;
     MOE_TRY(launch_topk(score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, logits, nullptr, bias, S.T, S.E, S.k,
-                        n_groups, topk_groups, tidx, tw, stream));
+                        n_groups, topk_groups, ridx, rw, stream, kc));
     if (!mark(2)) return MOE_ERR_CUDA;
   }
+  if (kc > 0)  // rerouting rounds: the serving expert of every slot and the served weights
+    MOE_TRY(launch_reroute(cand, cand_val, S.T, S.k, kc, S.E, capacity,
+                           score_fn == MOE_SCORE_SOFTMAX ? 0 : 1, chunk,
+                           reinterpret_cast<int*>(ws + L.prop), reinterpret_cast<int*>(ws + L.assign_c),
+                           reinterpret_cast<int*>(ws + L.next_c), reinterpret_cast<int*>(ws + L.fill),
+                           reinterpret_cast<int*>(ws + L.left), tidx, tw, dropped, stream));
   MOE_TRY(launch_dispatch(tidx, S.T, S.k, S.E, bf16 ? down_bn(S) : bn, bf16 ? down_tall_rows(S) : 0,
                           chunk, expert_counts, offsets, ntp,
                           bf16 ? gateup_bn(S) : 0, bf16 ? gateup_tall_rows(S) : 0,
-                          bf16 ? ntp2 : nullptr, capacity, dropped, sorted, slot, stream));
+                          bf16 ? ntp2 : nullptr, kc > 0 ? INT_MAX : capacity,
+                          kc > 0 ? nullptr : dropped, sorted, slot, stream));
   if (!mark(3)) return MOE_ERR_CUDA;
   // a gathering gate/up GEMM reads x through the permutation itself; otherwise (and for the
   // fp32 expert FFN) the permuted copy xs is written first

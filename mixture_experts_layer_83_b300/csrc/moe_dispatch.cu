@@ -14,7 +14,17 @@
 // With an expert capacity (page "Expert-Parallel MoE Inference", section "Capacity factor and
 // token dropping"), an assignment whose rank among its expert's assignments (token order) is
 // capacity or more is dropped: slot_pos = -1, no row in the permutation; expert_counts,
-// offsets and the tile prefixes count the dispatched assignments only.
+// offsets and the tile prefixes count the dispatched assignments only.  A negative expert id
+// (a slot that rerouting left without an expert) is dispatched nowhere either.
+//
+// Rerouting at capacity (the same section: overflow tokens are rerouted to their next-best
+// expert) runs in rounds over each token's kc candidates (its top-kc experts in selection
+// order): in round 0 slot j proposes candidate j; experts accept proposals in token order while
+// they have room; each rejected slot takes its token's next unused candidate for the next
+// round; a slot whose candidates run out is dropped.  A round is a histogram of the proposals,
+// a scan that compares them with each expert's room, a ranking that accepts or rejects each
+// proposal and a per-token step to the next candidates: the same stable counting sort as the
+// dispatch, so the outcome is deterministic.
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
@@ -32,7 +42,10 @@ __global__ void dispatch_count_kernel(const int* __restrict__ topk_idx, int R, i
   __syncthreads();
   const int base = blockIdx.x * kDispatchChunk;
   const int n = min(kDispatchChunk, R - base);
-  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[topk_idx[base + i]], 1);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = topk_idx[base + i];
+    if (e >= 0) atomicAdd(&hist[e], 1);
+  }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
 }
@@ -118,9 +131,10 @@ __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
   int* mine = wcount + warp * E;
   for (int r = 0; r < kPerWarp; r += 32) {
     const int i = base + r + lane;
-    const int e = i < R ? topk_idx[i] : -1 - lane;
+    const int e0 = i < R ? topk_idx[i] : -1;
+    const int e = e0 >= 0 ? e0 : -1 - lane;  // no expert: a key no other lane holds
     const unsigned peers = __match_any_sync(kFull, e);
-    if (i < R && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    if (e0 >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
     __syncwarp();
   }
   __syncthreads();
@@ -137,9 +151,12 @@ __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
   const unsigned lt = (1u << lane) - 1u;
   for (int r = 0; r < kPerWarp; r += 32) {
     const int i = base + r + lane;
-    const int e = i < R ? topk_idx[i] : -1 - lane;
+    const int e0 = i < R ? topk_idx[i] : -1;
+    const int e = e0 >= 0 ? e0 : -1 - lane;
     const unsigned peers = __match_any_sync(kFull, e);
-    if (i < R) {
+    if (i < R && e0 < 0) {
+      slot_pos[i] = -1;  // a slot without an expert
+    } else if (i < R) {
       const int rank = mine[e] + __popc(peers & lt);
       if (rank < capacity) {
         const int pos = offsets[e] + rank;
@@ -150,8 +167,165 @@ __global__ void __launch_bounds__(kDispatchWarps * 32) dispatch_scatter_kernel(
       }
     }
     __syncwarp();
-    if (i < R && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    if (e0 >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
     __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------ rerouting rounds
+// prop[i]: candidate index slot i proposes (-1: none, -2: rejected this round); assign_c[i]:
+// the accepted candidate index or -1; next_c[t]: the token's next unused candidate.
+__global__ void reroute_init_kernel(int T, int k, int E, int* __restrict__ prop,
+                                    int* __restrict__ assign_c, int* __restrict__ next_c,
+                                    int* __restrict__ fill) {
+  const int R = T * k;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < R; i += gridDim.x * blockDim.x) {
+    prop[i] = i % k;
+    assign_c[i] = -1;
+    if (i % k == 0) next_c[i / k] = k;
+    if (i < E) fill[i] = 0;
+  }
+  if (blockIdx.x == 0)
+    for (int e = R + threadIdx.x; e < E; e += blockDim.x) fill[e] = 0;
+}
+
+// The expert a slot proposes: its token's candidate prop[i], or -1.
+__device__ __forceinline__ int proposed_expert(const int* cand, const int* prop, int i, int k,
+                                               int kc) {
+  const int c = prop[i];
+  return c >= 0 ? cand[(size_t)(i / k) * kc + c] : -1;
+}
+
+__global__ void reroute_count_kernel(const int* __restrict__ cand, int kc,
+                                     const int* __restrict__ prop, int R, int k, int E,
+                                     int* __restrict__ chunk_counts) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kDispatchChunk;
+  const int n = min(kDispatchChunk, R - base);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = proposed_expert(cand, prop, base + i, k, kc);
+    if (e >= 0) atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Per expert: the chunk bases of this round's proposals (in place), the room before the round
+// (left) and the slots filled after it.
+__global__ void __launch_bounds__(1024) reroute_scan_kernel(int* __restrict__ chunk_counts,
+                                                            int nchunks, int E, int capacity,
+                                                            int* __restrict__ fill,
+                                                            int* __restrict__ left) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int tot = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const size_t o = (size_t)c * E + e;
+      const int v = chunk_counts[o];
+      chunk_counts[o] = tot;
+      tot += v;
+    }
+    const int room = capacity - fill[e] > 0 ? capacity - fill[e] : 0;
+    left[e] = room;
+    fill[e] += tot < room ? tot : room;
+  }
+}
+
+// A proposal is accepted when its rank among the round's proposals to its expert (token order)
+// is below the expert's room.
+__global__ void __launch_bounds__(kDispatchWarps * 32) reroute_accept_kernel(
+    const int* __restrict__ cand, int kc, int* __restrict__ prop, int R, int k, int E,
+    const int* __restrict__ chunk_base, const int* __restrict__ left, int* __restrict__ assign_c) {
+  extern __shared__ int wcount[];  // [kDispatchWarps][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) wcount[i] = 0;
+  __syncthreads();
+  constexpr int kPerWarp = kDispatchChunk / kDispatchWarps;
+  const int base = blockIdx.x * kDispatchChunk + warp * kPerWarp;
+  int* mine = wcount + warp * E;
+  for (int r = 0; r < kPerWarp; r += 32) {
+    const int i = base + r + lane;
+    const int e0 = i < R ? proposed_expert(cand, prop, i, k, kc) : -1;
+    const int e = e0 >= 0 ? e0 : -1 - lane;
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (e0 >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = chunk_base[(size_t)blockIdx.x * E + e];
+    for (int w = 0; w < kDispatchWarps; ++w) {
+      const int c = wcount[w * E + e];
+      wcount[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r = 0; r < kPerWarp; r += 32) {
+    const int i = base + r + lane;
+    const int e0 = i < R ? proposed_expert(cand, prop, i, k, kc) : -1;
+    const int e = e0 >= 0 ? e0 : -1 - lane;
+    const unsigned peers = __match_any_sync(kFull, e);
+    if (e0 >= 0) {
+      if (mine[e] + __popc(peers & lt) < left[e]) {
+        assign_c[i] = prop[i];
+        prop[i] = -1;
+      } else {
+        prop[i] = -2;
+      }
+    }
+    __syncwarp();
+    if (e0 >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Each rejected slot of a token, in slot order, takes the token's next unused candidate.
+__global__ void reroute_advance_kernel(int T, int k, int kc, int* __restrict__ prop,
+                                       int* __restrict__ next_c) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+    int nc = next_c[t];
+    for (int j = 0; j < k; ++j) {
+      const size_t i = (size_t)t * k + j;
+      if (prop[i] != -2) continue;
+      prop[i] = nc < kc ? nc++ : -1;
+    }
+    next_c[t] = nc;
+  }
+}
+
+// The serving expert of every slot (-1: dropped) and the gate weights renormalised over the
+// serving experts (softmax over their logits, or renormalised sigmoids); one warp per token.
+__global__ void reroute_finish_kernel(int T, int k, int kc, int src, const int* __restrict__ cand,
+                                      const float* __restrict__ cand_val,
+                                      const int* __restrict__ assign_c, int* __restrict__ topk_idx,
+                                      float* __restrict__ topk_w, int* __restrict__ dropped) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    const int c = lane < k ? assign_c[(size_t)t * k + lane] : -1;
+    const bool served = c >= 0;
+    const float v = served ? cand_val[(size_t)t * kc + c] : -INFINITY;
+    float s;
+    if (src == 0) {
+      float m = v;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+      s = served ? expf(v - m) : 0.f;
+    } else {
+      s = served ? 1.f / (1.f + expf(-v)) : 0.f;
+    }
+    float sum = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = served ? cand[(size_t)t * kc + c] : -1;
+      topk_w[(size_t)t * k + lane] = served ? s / sum : 0.f;
+    }
+    const unsigned miss = __ballot_sync(kFull, lane < k && !served);
+    if (dropped != nullptr && lane == 0 && miss != 0) atomicAdd(dropped, __popc(miss));
   }
 }
 
@@ -212,6 +386,36 @@ cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, in
   if (err != cudaSuccess) return err;
   dispatch_scatter_kernel<<<nchunks, kDispatchWarps * 32, kDispatchWarps * E * sizeof(int), s>>>(
       topk_idx, R, E, k, chunk_counts, offsets, capacity, sorted_token, slot_pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reroute(const int* cand, const float* cand_val, int T, int k, int kc, int E,
+                           int capacity, int src, int* chunk_counts, int* prop, int* assign_c,
+                           int* next_c, int* fill, int* left, int* topk_idx, float* topk_w,
+                           int* dropped, cudaStream_t s) {
+  const int R = T * k;
+  const int nchunks = (R + kDispatchChunk - 1) / kDispatchChunk;
+  int blocks = (R + 255) / 256;
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  if (blocks < 1) blocks = 1;
+  reroute_init_kernel<<<blocks, 256, 0, s>>>(T, k, E, prop, assign_c, next_c, fill);
+  cudaError_t err = cudaGetLastError();
+  // round 0 proposes the top-k; each later round at least one more candidate per token that
+  // still has a rejected slot, so kc - k + 1 rounds settle every slot
+  for (int round = 0; round <= kc - k && err == cudaSuccess; ++round) {
+    reroute_count_kernel<<<nchunks, 256, E * sizeof(int), s>>>(cand, kc, prop, R, k, E, chunk_counts);
+    reroute_scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, capacity, fill, left);
+    reroute_accept_kernel<<<nchunks, kDispatchWarps * 32, kDispatchWarps * E * sizeof(int), s>>>(
+        cand, kc, prop, R, k, E, chunk_counts, left, assign_c);
+    reroute_advance_kernel<<<(T + 255) / 256, 256, 0, s>>>(T, k, kc, prop, next_c);
+    err = cudaGetLastError();
+  }
+  if (err != cudaSuccess) return err;
+  if (dropped != nullptr && (err = cudaMemsetAsync(dropped, 0, sizeof(int), s)) != cudaSuccess) return err;
+  int wblocks = (T + 7) / 8;
+  if (wblocks > 148 * 32) wblocks = 148 * 32;
+  reroute_finish_kernel<<<wblocks, 256, 0, s>>>(T, k, kc, src, cand, cand_val, assign_c, topk_idx,
+                                                topk_w, dropped);
   return cudaGetLastError();
 }
 

@@ -110,6 +110,7 @@ struct RouterParams {
   int* counters;    // split reduction: [blocks] arrivals, zero when the kernel starts
   int* err;         // device status word
   int T, E, k, G, M, d;
+  int kc;           // > k: candidate mode ([T][kc] experts and raw values, for rerouting)
   int N;            // tokens per block: multiple of 16, at most 256
   int blocks, splits, kb_per_split, kblocks;
   int stages, b_stage_bytes;
@@ -126,8 +127,10 @@ cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int 
                                      float* logits, cudaStream_t s);
 // src: 0 = logits + softmax, 1 = logits + sigmoid, 2 = supplied key (a) and score (b).
 // G > 0: group-limited, M of G contiguous expert groups kept per token (G = 0: plain top-k).
+// kc > k: candidate mode, [T][kc] experts in selection order and their raw values.
 cudaError_t launch_topk(int src, const float* a, const float* b, const float* bias, int T, int E,
-                        int k, int G, int M, int* topk_idx, float* topk_w, cudaStream_t s);
+                        int k, int G, int M, int* topk_idx, float* topk_w, cudaStream_t s,
+                        int kc = 0);
 
 // Dispatch (moe_dispatch.cu).
 // ntp / ntp2 (either may be null): per-expert prefixes of tile units (seg_units) for n-tile
@@ -139,6 +142,16 @@ cudaError_t launch_dispatch(const int* topk_idx, int T, int k, int E, int bn, in
                             int tall2,
                             int* ntp2, int capacity, int* dropped, int* sorted_token,
                             int* slot_pos, cudaStream_t s);
+// Rerouting at capacity: from cand [T][kc] (experts in selection order) and their raw values,
+// rounds of proposals up to each expert's capacity; writes the serving expert of every slot
+// (-1: dropped) to topk_idx [T][k], the weights renormalised over the serving experts to
+// topk_w (src: 0 softmax logits, 1 sigmoid logits) and the number of dropped slots to *dropped
+// (may be null).  Scratch: chunk_counts as for the dispatch, prop / assign_c [T*k], next_c [T],
+// fill / left [E].
+cudaError_t launch_reroute(const int* cand, const float* cand_val, int T, int k, int kc, int E,
+                           int capacity, int src, int* chunk_counts, int* prop, int* assign_c,
+                           int* next_c, int* fill, int* left, int* topk_idx, float* topk_w,
+                           int* dropped, cudaStream_t s);
 // rows_dev (may be null): device row count replacing R (rows dispatched under a capacity).
 cudaError_t launch_gather(const void* x, const int* sorted_token, int R, const int* rows_dev,
                           int d, int elt_bytes, void* xs, cudaStream_t s);

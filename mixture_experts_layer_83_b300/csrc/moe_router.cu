@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
                                                    const float* __restrict__ b,
                                                    const float* __restrict__ bias, int T, int E,
                                                    int k, int G, int M, int* __restrict__ topk_idx,
-                                                   float* __restrict__ topk_w) {
+                                                   float* __restrict__ topk_w, int kc) {
+  const int ko = kc > k ? kc : k;  // outputs per token
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   float be[NV];  // this lane's experts' selection bias
@@ -58,23 +59,23 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ a,
       else
         taken |= 1u << v;
     }
-    select_topk<NV, SRC>(key, val, taken, E, k, G, M, topk_idx + (size_t)t * k,
-                         topk_w + (size_t)t * k);
+    select_topk<NV, SRC>(key, val, taken, E, k, G, M, topk_idx + (size_t)t * ko,
+                         topk_w + (size_t)t * ko, kc);
   }
 }
 
 template <int NV>
 cudaError_t launch_topk_nv(int src, const float* a, const float* b, const float* bias, int T,
-                           int E, int k, int G, int M, int* idx, float* w, cudaStream_t s) {
+                           int E, int k, int G, int M, int* idx, float* w, int kc, cudaStream_t s) {
   const int threads = 256, wpb = threads / 32;
   int blocks = (T + wpb - 1) / wpb;
   if (blocks > 148 * 32) blocks = 148 * 32;
   if (src == 0)
-    topk_kernel<NV, 0><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w);
+    topk_kernel<NV, 0><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w, kc);
   else if (src == 1)
-    topk_kernel<NV, 1><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w);
+    topk_kernel<NV, 1><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w, kc);
   else
-    topk_kernel<NV, 2><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w);
+    topk_kernel<NV, 2><<<blocks, threads, 0, s>>>(a, b, bias, T, E, k, G, M, idx, w, kc);
   return cudaGetLastError();
 }
 
@@ -90,14 +91,14 @@ cudaError_t launch_router_logits_f32(const float* x, const float* w_router, int 
 }
 
 cudaError_t launch_topk(int src, const float* a, const float* b, const float* bias, int T, int E,
-                        int k, int G, int M, int* topk_idx, float* topk_w, cudaStream_t s) {
+                        int k, int G, int M, int* topk_idx, float* topk_w, cudaStream_t s, int kc) {
   const int nv = (E + 31) / 32;
-  if (nv <= 1) return launch_topk_nv<1>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
-  if (nv <= 2) return launch_topk_nv<2>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
-  if (nv <= 4) return launch_topk_nv<4>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
-  if (nv <= 8) return launch_topk_nv<8>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
-  if (nv <= 16) return launch_topk_nv<16>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
-  return launch_topk_nv<32>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, s);
+  if (nv <= 1) return launch_topk_nv<1>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, kc, s);
+  if (nv <= 2) return launch_topk_nv<2>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, kc, s);
+  if (nv <= 4) return launch_topk_nv<4>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, kc, s);
+  if (nv <= 8) return launch_topk_nv<8>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, kc, s);
+  if (nv <= 16) return launch_topk_nv<16>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, kc, s);
+  return launch_topk_nv<32>(src, a, b, bias, T, E, k, G, M, topk_idx, topk_w, kc, s);
 }
 
 }  // namespace moe

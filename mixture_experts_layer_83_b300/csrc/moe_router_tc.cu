@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
   __syncthreads();
 
   // ------------------------------------------------------------------ selection
+  const int ko = p.kc > p.k ? p.kc : p.k;  // outputs per token
   float be[NV];  // this lane's experts' selection bias
 #pragma unroll
   for (int vv = 0; vv < NV; ++vv) {
@@ -262,8 +263,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
           if (e < p.E) select_key<SRC>(L[il * 256 + e], 0.f, be[vv], key[vv], val[vv]);
           else taken |= 1u << vv;
         }
-        select_topk<NV, SRC>(key, val, taken, p.E, p.k, p.G, p.M, p.topk_idx + (size_t)t * p.k,
-                             p.topk_w + (size_t)t * p.k);
+        select_topk<NV, SRC>(key, val, taken, p.E, p.k, p.G, p.M, p.topk_idx + (size_t)t * ko,
+                             p.topk_w + (size_t)t * ko, p.kc);
       }
     }
   } else {
@@ -310,8 +311,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
             if (e < p.E) select_key<SRC>(lg[vv], 0.f, be[vv], key[vv], val[vv]);
             else taken |= 1u << vv;
           }
-          select_topk<NV, SRC>(key, val, taken, p.E, p.k, p.G, p.M, p.topk_idx + (size_t)t * p.k,
-                               p.topk_w + (size_t)t * p.k);
+          select_topk<NV, SRC>(key, val, taken, p.E, p.k, p.G, p.M, p.topk_idx + (size_t)t * ko,
+                               p.topk_w + (size_t)t * ko, p.kc);
         }
       }
     }

@@ -49,10 +49,14 @@ __device__ __forceinline__ void select_key(float a, float b, float bias_e, float
 // butterfly of shuffles agrees on the warp's best, the owning lane marks it taken and lane r
 // keeps round r's winner.  Lanes r < k write expert r of the token (key-descending order) and
 // its renormalised gate weight to out_idx[r], out_w[r].
+// Candidate mode (kc > k, for rerouting at an expert capacity): kc rounds, and lanes r < kc
+// write expert r and its raw value (no renormalisation) instead.
 template <int NV, int SRC>
 __device__ __forceinline__ void select_topk(const float (&key)[NV], const float (&val)[NV],
                                             uint32_t taken, int E, int k, int G, int M,
-                                            int* out_idx, float* out_w) {
+                                            int* out_idx, float* out_w, int kc = 0) {
+  const bool cands = kc > k;
+  const int rounds = cands ? kc : k;
   constexpr unsigned kFull = 0xFFFFFFFFu;
   const int lane = threadIdx.x & 31;
   if (G > 0) {
@@ -93,7 +97,7 @@ __device__ __forceinline__ void select_topk(const float (&key)[NV], const float 
   }
   int my_e = 0;
   float my_val = 0.f;
-  for (int r = 0; r < k; ++r) {
+  for (int r = 0; r < rounds; ++r) {
     float bk = -INFINITY;
     int be = INT_MAX;
 #pragma unroll
@@ -124,6 +128,13 @@ __device__ __forceinline__ void select_topk(const float (&key)[NV], const float 
       my_e = be;
       my_val = wval;
     }
+  }
+  if (cands) {
+    if (lane < kc) {
+      out_idx[lane] = my_e;
+      out_w[lane] = my_val;
+    }
+    return;
   }
   float s;
   if (SRC == 0) {

@@ -54,7 +54,7 @@ def gpu_forward(cfg, dev, stream=None, workspace=None, stage_events=None):
                           c["score"], dev.get("bias"), shared, out, counts, workspace, ws_bytes,
                           stream, tidx, tw, st, stage_events=stage_events,
                           capacity_factor=cf, dropped=dropped if cf > 0 else None,
-                          **group_args(c))
+                          reroute=c.get("reroute", 0), **group_args(c))
     return dict(out=out, counts=counts, topk_idx=tidx, topk_w=tw, sorted_token=st,
                 dropped=dropped[:1], workspace=workspace)
 
@@ -149,6 +149,30 @@ def check_dispatch(cfg, g_idx, g_counts, g_sorted, g_dropped=None):
     np.testing.assert_array_equal(g_counts, counts)
     np.testing.assert_array_equal(g_sorted, st)
     return counts, np.ones(g_idx.shape, dtype=bool)
+
+
+def check_reroute(cfg, key, score, g_idx, g_counts, g_sorted, g_dropped):
+    """Rerouting at capacity, checked on the GPU's own assignment (the rounds can cascade from
+    one near-tie in a candidate order, so at full size the exact decisions are not compared):
+    every serving expert is among its token's top-(k + reroute) oracle keys up to MARGIN, a
+    token's serving experts are distinct, no expert is over capacity, served + dropped = T*k,
+    and the dispatch tables are the stable counting sort of the assignment.  Returns the
+    oracle weights renormalised over the GPU's serving experts."""
+    c = configs.get(cfg)
+    T, E, k = c["T"], c["E"], c["k"]
+    kc = k + c["reroute"]
+    cap = oracle.capacity(T, E, k, c["capacity_factor"])
+    assert g_counts.max() <= cap
+    assert int(g_counts.sum()) + int(g_dropped[0]) == T * k
+    kth = -np.sort(-key, axis=1)[:, kc - 1]   # the kc-th largest oracle key of each token
+    for t in range(T):
+        served = g_idx[t][g_idx[t] >= 0]
+        assert len(set(served.tolist())) == len(served), f"token {t}: expert served twice"
+        assert np.all(key[t, served] >= kth[t] - MARGIN), f"token {t}: expert beyond its candidates"
+    want = [t for e in range(E) for t in range(T) for j in range(k) if g_idx[t, j] == e]
+    np.testing.assert_array_equal(g_sorted[:len(want)], want)
+    np.testing.assert_array_equal(g_counts, np.bincount(g_idx[g_idx >= 0], minlength=E))
+    return oracle.served_weights(score, g_idx)
 
 
 def check_output(cfg, got, ref):
@@ -314,10 +338,18 @@ def sampled_check(cfg, dev, n_sample=1024, threads=None, seed=0):
     wr = _host_elems(dev["w_router"])
     bias = dev["bias"].cpu().numpy() if "bias" in dev else None
     key, score, o_idx, margin = oracle_routing(c, x, wr, bias, threads)
-    n_ex, w_ref = check_routing(c, key, score, margin, o_idx, res["topk_idx"], res["topk_w"])
-    counts, kept = check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"],
-                                  res["dropped"])
-    w_ref = np.where(kept, w_ref, 0.0)   # a dropped assignment contributes nothing
+    if c.get("reroute", 0) > 0:
+        n_ex = 0
+        w_ref = check_reroute(c, key, score, res["topk_idx"], res["counts"], res["sorted_token"],
+                              res["dropped"])
+        np.testing.assert_allclose(res["topk_w"], w_ref, rtol=0, atol=2e-5)
+        counts, kept = res["counts"], res["topk_idx"] >= 0
+        res["topk_idx"] = np.where(kept, res["topk_idx"], 0)   # weight 0: contributes nothing
+    else:
+        n_ex, w_ref = check_routing(c, key, score, margin, o_idx, res["topk_idx"], res["topk_w"])
+        counts, kept = check_dispatch(c, res["topk_idx"], res["counts"], res["sorted_token"],
+                                      res["dropped"])
+        w_ref = np.where(kept, w_ref, 0.0)   # a dropped assignment contributes nothing
     T, k = c["T"], c["k"]
     edges = {}
     if n_sample >= T:

@@ -305,3 +305,13 @@ def test_error_path_diagnostics_check_arguments_before_launching():
     for ws, limit in ((None, 10_000), (20, 10_000), (256, 999), (256, 1_000_000_001)):
         assert moe.moe_debug_wait_timeout(ws, limit, stream=0, check=False) == \
             moe.MOE_ERR_INVALID_ARG
+
+
+def test_reroute_option_checked_before_launching():
+    """Rerouting needs a capacity, at most 32 candidates per token and no more than E; the
+    checks run on the host before anything is enqueued."""
+    for kw in (dict(reroute=2), dict(capacity_factor=1.0, reroute=-1),
+               dict(capacity_factor=1.0, reroute=7), dict(capacity_factor=1.0, reroute=31)):
+        rc = moe.moe_layer_forward(shape(), 16, 16, 16, 16, moe.MOE_SCORE_SOFTMAX, None, None, 16,
+                                   16, 16, 1 << 40, stream=0, check=False, **kw)
+        assert rc == moe.MOE_ERR_INVALID_ARG, kw

@@ -59,3 +59,17 @@ def test_full_size_skewed_layer_with_capacity():
     assert stats["dropped"] > 0
     del dev
     torch.cuda.empty_cache()
+
+
+def test_full_size_skewed_layer_with_capacity_and_rerouting():
+    """The Zipf-skewed layer with a capacity factor of 1.25 and up to 4 next-best experts per
+    token: overflow of the hot experts moves to colder ones; the GPU's assignment is checked
+    for validity (serving experts among each token's top-12, capacity, tables) and sampled
+    outputs against the oracle under that assignment."""
+    c = dict(configs.CONFIGS[4], capacity_factor=1.25, reroute=4)
+    dev = moe_inputs.device_inputs(c)
+    torch.cuda.synchronize()
+    stats = sampled_check(c, dev, n_sample=SAMPLE[4])
+    print(c["name"], "capacity 1.25 + reroute 4", stats)
+    del dev
+    torch.cuda.empty_cache()

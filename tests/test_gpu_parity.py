@@ -232,3 +232,40 @@ def test_kernel_clock_records():
     res = gpu_forward(c32, moe_inputs.upload(c32, moe_inputs.host_inputs(c32)))
     torch.cuda.synchronize()
     assert all(v == (0.0, 0.0) for v in moe.moe_workspace_kernel_clocks(res["workspace"]).values())
+
+
+@pytest.mark.parametrize("score,k,extra,cf,Fs,seed", [(SOFTMAX, 2, 2, 1.0, 0, 201),
+                                                      (SIGMOID, 4, 4, 1.0, 64, 228),
+                                                      (SOFTMAX, 1, 3, 1.0, 0, 201),
+                                                      (SIGMOID, 2, 6, 0.75, 64, 228),
+                                                      (SOFTMAX, 4, 2, 0.8, 64, 201)])
+def test_reroute_matches_oracle(score, k, extra, cf, Fs, seed):
+    """Rerouting at capacity, bit-exact against the oracle on the same inputs: the serving
+    expert of every slot (-1: dropped), expert counts, the permutation and the number dropped;
+    the served weights and the layer output within tolerance.  The inputs are such that no
+    token has a near-tie (1e-4) within its top-(k + extra + 1) keys, so both sides see the same
+    candidate order."""
+    import mixture_experts_layer_83_b300 as moe
+    c = make_shape(T=300, d=256, E=16, k=k, F=128, Fs=Fs, dtype="bf16", score=score,
+                   bias_range=0.01 if score == SIGMOID else 0.0, seed=seed, name="reroute")
+    c.update(capacity_factor=cf, reroute=extra)
+    host = moe_inputs.host_inputs(c)
+    res = to_host(gpu_forward(c, moe_inputs.upload(c, host)))
+    _, sc, key = oracle.router_scores(host["x"], host["w_router"], c["score"], host.get("bias"))
+    kc = k + extra
+    cand, _, _ = oracle.topk(key, sc, kc)
+    srt = -np.sort(-key, axis=1)[:, :kc + 1]
+    assert np.min(srt[:, :-1] - srt[:, 1:]) >= 1e-4, "inputs with a near-tie: pick another seed"
+    cap = oracle.capacity(c["T"], c["E"], k, cf)
+    assign, _, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, k, c["E"], cap)
+    np.testing.assert_array_equal(res["topk_idx"], assign)
+    np.testing.assert_array_equal(res["counts"], counts)
+    np.testing.assert_array_equal(res["sorted_token"][:offsets[-1]], st)
+    assert int(res["dropped"][0]) == dropped
+    w = oracle.served_weights(sc, assign)
+    np.testing.assert_allclose(res["topk_w"], w, rtol=0, atol=2e-5)
+    experts = {e: (host["w_gate_up"][e], host["w_down"][e]) for e in range(c["E"])}
+    shared = (host["sh_gate_up"], host["sh_down"]) if Fs > 0 else None
+    from layer_check import check_output, oracle_rows
+    ref = oracle_rows(c, host["x"], np.where(assign >= 0, assign, 0), w, experts, shared, 4)
+    print(check_output(c, res["out"], ref), "rerouted+dropped:", dropped, "counts max", counts.max(), cap)
