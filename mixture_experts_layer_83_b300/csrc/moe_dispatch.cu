@@ -75,6 +75,53 @@ __device__ int block_inclusive_scan(int v, int* scratch) {
   return v + add;
 }
 
+// Per expert e < E: rewrites the chunk histogram chunk_counts[c][e] (c < nchunks) as exclusive
+// prefixes over the chunks (token order) and leaves the expert's total in tot_s[e].  The
+// block's 1024 threads split into G = 1024 / E' threads per expert (E' = E rounded up to a
+// power of two), each over a contiguous run of chunks: the loads of a run are independent of
+// one another, and the only serial step is a scan over the G partial sums in shared memory.
+// part and tot_s hold 1024 ints each.
+__device__ void chunk_scan(int* __restrict__ chunk_counts, int nchunks, int E, int* part, int* tot_s) {
+  int ep = 1;
+  while (ep < E) ep <<= 1;
+  const int G = 1024 / ep;
+  const int g = threadIdx.x / ep, e = threadIdx.x % ep;
+  const int per = (nchunks + G - 1) / G;
+  const int c0 = g * per, c1 = min(nchunks, c0 + per);
+  const bool active = e < E && g < G;
+  if (active) {
+    int sum = 0;
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) sum += chunk_counts[(size_t)c * E + e];
+    part[g * ep + e] = sum;
+  }
+  __syncthreads();
+  if (active && g == 0) {
+    int run = 0;
+    for (int x = 0; x < G; ++x) {
+      const int v = part[x * ep + e];
+      part[x * ep + e] = run;
+      run += v;
+    }
+    tot_s[e] = run;
+  }
+  __syncthreads();
+  if (active) {
+    int run = part[g * ep + e];
+    for (int c = c0; c < c1; c += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = c + j < c1 ? chunk_counts[(size_t)(c + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c + j < c1) {
+          chunk_counts[(size_t)(c + j) * E + e] = run;
+          run += v[j];
+        }
+    }
+  }
+}
+
 // ntp / ntp2: prefixes of the tile units per expert (seg_units) for n-tile caps bn / bn2 and
 // tall-tile limits tall / tall2 (the two grouped GEMMs may tile the token rows differently);
 // either may be null.
@@ -86,16 +133,10 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int* __restrict__ c
                                                              int tall2, int* __restrict__ ntp2,
                                                              int capacity, int* __restrict__ dropped) {
   __shared__ int scratch[32];
+  __shared__ int part[1024], tot_s[1024];
+  chunk_scan(chunk_counts, nchunks, E, part, tot_s);
   const int e = threadIdx.x;
-  int tot = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const size_t o = (size_t)c * E + e;
-      const int v = chunk_counts[o];
-      chunk_counts[o] = tot;
-      tot += v;
-    }
-  }
+  int tot = e < E ? tot_s[e] : 0;
   const int routed = tot;
   tot = tot < capacity ? tot : capacity;  // dispatched assignments
   const int nt = seg_units(tot, bn, tall);
@@ -218,14 +259,10 @@ __global__ void __launch_bounds__(1024) reroute_scan_kernel(int* __restrict__ ch
                                                             int nchunks, int E, int capacity,
                                                             int* __restrict__ fill,
                                                             int* __restrict__ left) {
+  __shared__ int part[1024], tot_s[1024];
+  chunk_scan(chunk_counts, nchunks, E, part, tot_s);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int tot = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const size_t o = (size_t)c * E + e;
-      const int v = chunk_counts[o];
-      chunk_counts[o] = tot;
-      tot += v;
-    }
+    const int tot = tot_s[e];
     const int room = capacity - fill[e] > 0 ? capacity - fill[e] : 0;
     left[e] = room;
     fill[e] += tot < room ? tot : room;
