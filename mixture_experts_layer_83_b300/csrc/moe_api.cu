@@ -458,6 +458,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   if (reroute < 0 || (reroute > 0 && capacity == INT_MAX) || s->k + reroute > kMaxK ||
       s->k + reroute > s->E)
     return MOE_ERR_INVALID_ARG;
+  // under group-limited routing every candidate comes from the kept groups
+  if (reroute > 0 && n_groups > 0 && s->k + reroute > topk_groups * (s->E / n_groups))
+    return MOE_ERR_INVALID_ARG;
   const int kc = reroute > 0 ? s->k + reroute : 0;
   int* dropped = opts ? opts->dropped : nullptr;
   if (dropped != nullptr && !aligned16(dropped)) return MOE_ERR_INVALID_ARG;

@@ -311,7 +311,9 @@ def test_reroute_option_checked_before_launching():
     """Rerouting needs a capacity, at most 32 candidates per token and no more than E; the
     checks run on the host before anything is enqueued."""
     for kw in (dict(reroute=2), dict(capacity_factor=1.0, reroute=-1),
-               dict(capacity_factor=1.0, reroute=7), dict(capacity_factor=1.0, reroute=31)):
+               dict(capacity_factor=1.0, reroute=7), dict(capacity_factor=1.0, reroute=31),
+               # 2 of 4 groups keep 4 of the 8 experts: 2 + 3 candidates do not fit
+               dict(capacity_factor=1.0, reroute=3, n_groups=4, topk_groups=2)):
         rc = moe.moe_layer_forward(shape(), 16, 16, 16, 16, moe.MOE_SCORE_SOFTMAX, None, None, 16,
                                    16, 16, 1 << 40, stream=0, check=False, **kw)
         assert rc == moe.MOE_ERR_INVALID_ARG, kw

@@ -269,3 +269,40 @@ def test_reroute_matches_oracle(score, k, extra, cf, Fs, seed):
     from layer_check import check_output, oracle_rows
     ref = oracle_rows(c, host["x"], np.where(assign >= 0, assign, 0), w, experts, shared, 4)
     print(check_output(c, res["out"], ref), "rerouted+dropped:", dropped, "counts max", counts.max(), cap)
+
+
+@pytest.mark.parametrize("score,k,extra,Fs,E,G,M,seed", [(SOFTMAX, 2, 2, 0, 16, 4, 2, 302),
+                                                       (SIGMOID, 4, 3, 64, 32, 8, 3, 319)])
+def test_reroute_with_groups_matches_oracle(score, k, extra, Fs, E, G, M, seed):
+    """Rerouting under group-limited routing: the candidates are the token's top-(k + extra)
+    experts of its kept groups, bit-exact against the oracle's grouped top-k and rounds.  The
+    inputs have no near-tie (1e-4) among the kept groups' top-(k + extra + 1) keys nor between
+    the M-th and (M+1)-th group scores."""
+    c = make_shape(T=300, d=256, E=E, k=k, F=128, Fs=Fs, dtype="bf16", score=score,
+                   bias_range=0.01 if score == SIGMOID else 0.0, seed=seed, name="reroute")
+    c.update(capacity_factor=1.0, reroute=extra, groups=G, topk_groups=M)
+    host = moe_inputs.host_inputs(c)
+    res = to_host(gpu_forward(c, moe_inputs.upload(c, host)))
+    _, sc, key = oracle.router_scores(host["x"], host["w_router"], c["score"], host.get("bias"))
+    kc = k + extra
+    gs = key.reshape(len(key), G, E // G).max(axis=2)
+    gsrt = -np.sort(-gs, axis=1)
+    assert np.min(gsrt[:, M - 1] - gsrt[:, M]) >= 1e-4, "group scores with a near-tie"
+    cand, _, _ = oracle.topk_grouped(key, sc, kc + 1, G, M)
+    kept = np.take_along_axis(key, cand.astype(np.int64), axis=1)
+    assert np.min(kept[:, :-1] - kept[:, 1:]) >= 1e-4, "keys with a near-tie"
+    cand = np.ascontiguousarray(cand[:, :kc])
+    cap = oracle.capacity(c["T"], E, k, 1.0)
+    assign, _, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, k, E, cap)
+    assert ((assign >= 0) & (assign != cand[:, :k])).any(), "no slot was rerouted"
+    np.testing.assert_array_equal(res["topk_idx"], assign)
+    np.testing.assert_array_equal(res["counts"], counts)
+    np.testing.assert_array_equal(res["sorted_token"][:offsets[-1]], st)
+    assert int(res["dropped"][0]) == dropped
+    w = oracle.served_weights(sc, assign)
+    np.testing.assert_allclose(res["topk_w"], w, rtol=0, atol=2e-5)
+    experts = {e: (host["w_gate_up"][e], host["w_down"][e]) for e in range(E)}
+    shared = (host["sh_gate_up"], host["sh_down"]) if Fs > 0 else None
+    from layer_check import check_output, oracle_rows
+    ref = oracle_rows(c, host["x"], np.where(assign >= 0, assign, 0), w, experts, shared, 4)
+    print(check_output(c, res["out"], ref))
