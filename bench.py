@@ -11,8 +11,8 @@ reported under "decode".
 
 Under torchrun each rank runs an independent replica on its own tokens (data parallel, no
 collective on the data path); the time is the max over ranks and the value counts the tokens
-of all ranks.  ``--impl reference`` times the fp64 CPU oracle (the reference of this build)
-on a bounded sample of the same workload, on rank 0 only.
+of all ranks.  ``--impl reference`` times the fp64 CPU oracle (the reference arm) on a
+bounded sample of the same workload, on rank 0 only.
 """
 import argparse
 import json

@@ -143,9 +143,10 @@ typedef struct {
    * next-best expert); needs capacity_factor > 0.  reroute = the candidates each token may
    * take beyond its top-k (its next-best experts in selection order; k + reroute <= 32 and
    * <= E; with group-limited routing the candidates come from the kept groups only, and
-   * k + reroute <= topk_groups * E / n_groups).  In round 0 every token's k slots propose its top-k; an expert accepts proposals in
-   * token order while it has room; each rejected slot takes its token's next unused candidate
-   * and proposes it in the next round; a slot whose candidates run out is dropped.  The gate
+   * k + reroute <= topk_groups * E / n_groups).  In round 0 every token's k slots propose
+   * its top-k; an expert accepts proposals in token order while it has room; each rejected
+   * slot takes its token's next unused candidate and proposes it in the next round; a slot
+   * whose candidates run out is dropped.  The gate
    * weights are renormalised over the experts that serve the token.  topk_idx_out then holds
    * the serving expert of every slot (-1: dropped) and topk_w_out those weights.  0: drop. */
   int reroute;

@@ -35,8 +35,8 @@ constexpr int kMaxDevices = 64;
 
 using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
-// The driver's cuCtxGetCurrent, reached through the runtime (the library links no driver
-// library directly).
+// The CUDA driver API's cuCtxGetCurrent, reached through the runtime (the library links no
+// driver library directly).
 CtxGetCurrentFn ctx_get_current() {
   static CtxGetCurrentFn fn = nullptr;
   static std::once_flag once;
