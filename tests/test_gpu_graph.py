@@ -36,6 +36,9 @@ CASES = {
     "bf16_groups_capacity": dict(make_shape(512, 128, 16, 4, 128, score=SIGMOID,
                                             bias_range=0.01, seed=34, groups=4),
                                  topk_groups=2, capacity_factor=1.0),
+    # rerouting of the overflow at an expert capacity: its fixed number of rounds is captured too
+    "bf16_reroute": dict(make_shape(400, 128, 16, 2, 128, Fs=64, score=SOFTMAX, seed=35),
+                         capacity_factor=1.0, reroute=3),
     # true-fp32 CUDA-core path
     "f32_ragged": make_shape(33, 70, 5, 2, 33, Fs=17, dtype="f32", seed=33),
 }
@@ -69,7 +72,8 @@ def test_forward_replays_from_a_cuda_graph(name):
         moe.moe_layer_forward(shape, x, dev["w_router"], dev["w_gate_up"], dev["w_down"],
                               cfg["score"], dev.get("bias"), shared, out, counts, ws, ws_bytes,
                               None, tidx, tw, st, capacity_factor=cf,
-                              dropped=dropped if cf > 0 else None, **group_args(cfg))
+                              dropped=dropped if cf > 0 else None, reroute=cfg.get("reroute", 0),
+                              **group_args(cfg))
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
