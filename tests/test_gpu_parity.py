@@ -271,6 +271,40 @@ def test_reroute_matches_oracle(score, k, extra, cf, Fs, seed):
     print(check_output(c, res["out"], ref), "rerouted+dropped:", dropped, "counts max", counts.max(), cap)
 
 
+@pytest.mark.parametrize("dtype,score,T,E,cf,seed", [("f32", SOFTMAX, 300, 16, 1.0, 402),
+                                                      ("bf16", SOFTMAX, 96, 272, 0.5, 402),
+                                                      ("bf16", SIGMOID, 96, 272, 0.5, 509)])
+def test_reroute_unfused_router_matches_oracle(dtype, score, T, E, cf, seed):
+    """Rerouting where the candidates come from the top-k kernel rather than the fused router:
+    the fp32 layer (CUDA-core router GEMM) and a bf16 layer with more than 256 experts (the
+    tensor-core router GEMM writes logits); top-2 with 2 more candidates, bit-exact against the
+    oracle on inputs with no near-tie among each token's top-5 keys."""
+    k, extra = 2, 2
+    c = make_shape(T=T, d=128, E=E, k=k, F=64, Fs=0, dtype=dtype, score=score,
+                   bias_range=0.01 if score == SIGMOID else 0.0, seed=seed, name="reroute")
+    c.update(capacity_factor=cf, reroute=extra)
+    host = moe_inputs.host_inputs(c)
+    res = to_host(gpu_forward(c, moe_inputs.upload(c, host)))
+    _, sc, key = oracle.router_scores(host["x"], host["w_router"], c["score"], host.get("bias"))
+    kc = k + extra
+    srt = -np.sort(-key, axis=1)[:, :kc + 1]
+    assert np.min(srt[:, :-1] - srt[:, 1:]) >= 1e-4, "inputs with a near-tie: pick another seed"
+    cand, _, _ = oracle.topk(key, sc, kc)
+    cap = oracle.capacity(T, E, k, cf)
+    assign, _, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, k, E, cap)
+    assert ((assign >= 0) & (assign != cand[:, :k])).any(), "no slot was rerouted"
+    np.testing.assert_array_equal(res["topk_idx"], assign)
+    np.testing.assert_array_equal(res["counts"], counts)
+    np.testing.assert_array_equal(res["sorted_token"][:offsets[-1]], st)
+    assert int(res["dropped"][0]) == dropped
+    w = oracle.served_weights(sc, assign)
+    np.testing.assert_allclose(res["topk_w"], w, rtol=0, atol=2e-5)
+    experts = {e: (host["w_gate_up"][e], host["w_down"][e]) for e in range(E)}
+    from layer_check import check_output, oracle_rows
+    ref = oracle_rows(c, host["x"], np.where(assign >= 0, assign, 0), w, experts, None, 4)
+    print(check_output(c, res["out"], ref))
+
+
 @pytest.mark.parametrize("score,k,extra,Fs,E,G,M,seed", [(SOFTMAX, 2, 2, 0, 16, 4, 2, 302),
                                                        (SIGMOID, 4, 3, 64, 32, 8, 3, 319)])
 def test_reroute_with_groups_matches_oracle(score, k, extra, Fs, E, G, M, seed):
