@@ -271,6 +271,32 @@ def test_reroute_matches_oracle(score, k, extra, cf, Fs, seed):
     print(check_output(c, res["out"], ref), "rerouted+dropped:", dropped, "counts max", counts.max(), cap)
 
 
+@pytest.mark.parametrize("T,E,k,extra,cf,seed", [(48, 32, 4, 28, 0.5, 501),
+                                                  (64, 8, 2, 6, 0.9, 501)])
+def test_reroute_at_the_candidate_limits(T, E, k, extra, cf, seed):
+    """Rerouting with the most candidates the options allow: k + extra = 32 (the selection's
+    limit, 28 rounds after the first) and k + extra = E (every expert a candidate); bit-exact
+    against the oracle on inputs whose candidate keys have no near-tie."""
+    c = make_shape(T=T, d=128, E=E, k=k, F=64, Fs=0, dtype="bf16", score=SOFTMAX, seed=seed,
+                   name="reroute")
+    c.update(capacity_factor=cf, reroute=extra)
+    host = moe_inputs.host_inputs(c)
+    res = to_host(gpu_forward(c, moe_inputs.upload(c, host)))
+    _, sc, key = oracle.router_scores(host["x"], host["w_router"], c["score"], host.get("bias"))
+    kc = k + extra
+    srt = -np.sort(-key, axis=1)[:, :kc + 1]
+    assert np.min(srt[:, :-1] - srt[:, 1:]) >= 1e-4, "inputs with a near-tie: pick another seed"
+    cand, _, _ = oracle.topk(key, sc, kc)
+    cap = oracle.capacity(T, E, k, cf)
+    assign, _, counts, offsets, st, sp, dropped = oracle.dispatch_reroute(cand, k, E, cap)
+    assert ((assign >= 0) & (assign != cand[:, :k])).any(), "no slot was rerouted"
+    np.testing.assert_array_equal(res["topk_idx"], assign)
+    np.testing.assert_array_equal(res["counts"], counts)
+    np.testing.assert_array_equal(res["sorted_token"][:offsets[-1]], st)
+    assert int(res["dropped"][0]) == dropped
+    np.testing.assert_allclose(res["topk_w"], oracle.served_weights(sc, assign), rtol=0, atol=2e-5)
+
+
 @pytest.mark.parametrize("dtype,score,T,E,cf,seed", [("f32", SOFTMAX, 300, 16, 1.0, 402),
                                                       ("bf16", SOFTMAX, 96, 272, 0.5, 402),
                                                       ("bf16", SIGMOID, 96, 272, 0.5, 509)])
