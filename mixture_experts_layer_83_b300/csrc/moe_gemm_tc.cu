@@ -466,7 +466,9 @@ __global__ void __launch_bounds__(threads_of<MODE, CG, WIDE>(), ctas_per_sm<CG, 
         const uint32_t idesc = idesc_bf16_f32(128 * CG, nh > 0 ? nh : 16);
         const int kblocks = P.K >> 6;
         for (int kb = 0; kb < kblocks; ++kb) {
-          // every issuer waits for every stage of the k-step and releases each of them
+          // the issuers share the token stage; a wide tile's weight stage too, while a tall tile
+          // gives each issuer a weight stage of its own, which it alone waits for and releases
+          // (committing twice: a weight stage's empty barrier counts one arrival per issuer)
           int ast[2];
           uint32_t aph[2];
           for (int x = 0; x < parts; ++x) {
@@ -477,23 +479,24 @@ __global__ void __launch_bounds__(threads_of<MODE, CG, WIDE>(), ctas_per_sm<CG, 
               pa ^= 1u;
             }
           }
-          bool got = mbar_wait(&full_b[sb], pb, abort_flag, p.err, kErrMmaWait);
-          for (int x = 0; x < parts && got; ++x)
-            got = mbar_wait(&full_a[ast[x]], aph[x], abort_flag, p.err, kErrMmaWait);
+          const int own = WIDE && tl.tall ? h : 0;  // the weight stage this issuer reads
+          const bool got = mbar_wait(&full_b[sb], pb, abort_flag, p.err, kErrMmaWait) &&
+                           mbar_wait(&full_a[ast[own]], aph[own], abort_flag, p.err, kErrMmaWait);
           if (!got) {
             ok = false;
             break;
           }
           tc_fence_after();
           if (nh > 0) {
-            const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)ast[tl.tall ? h : 0] * kABytes));
+            const uint64_t ad = sdesc_k_sw128(smem_u32(ring_a + (size_t)ast[own] * kABytes));
             const uint64_t bd =
                 sdesc_k_sw128(smem_u32(ring_b + (size_t)sb * p.b_stage_bytes + (size_t)brow * 128));
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mma_bf16<CG>(d_tmem, ad + 2ull * j, bd + 2ull * j, idesc, (kb | j) != 0 ? 1u : 0u);
           }
-          for (int x = 0; x < parts; ++x) mma_commit<CG>(&empty_a[ast[x]]);
+          mma_commit<CG>(&empty_a[ast[own]]);
+          if (WIDE && tl.tall) mma_commit<CG>(&empty_a[ast[own]]);
           mma_commit<CG>(&empty_b[sb]);
           if (++sb == SB) {
             sb = 0;
@@ -822,6 +825,9 @@ cudaError_t launch_gemm_tc(int mode, const TcParams& p, int sms, cudaStream_t s)
   // the forms this library uses: router on one CTA, gate/up on wide pairs, down on pairs
   if (mode == kModeRouter && p.cg == 1 && !p.wide) return launch_single<kModeRouter>(p, sms, smem, s);
   if (mode != kModeGateUp && p.gather != 0) return cudaErrorInvalidConfiguration;
+  // tall tiles need the two MMA issuers of the wide pair form
+  if ((p.prob[0].tall_rows > 0 || p.prob[1].tall_rows > 0) && !(p.cg == 2 && p.wide))
+    return cudaErrorInvalidConfiguration;
   if (mode == kModeGateUp && p.cg == 2 && p.wide && p.bn <= 2 * kAccCols)
     return launch_pair<kModeGateUp, 1>(p, sms, smem, s);
   if (mode == kModeGateUp && p.cg == 2 && !p.wide && p.bn <= kAccCols)
