@@ -30,7 +30,9 @@
 //   warp 1 lane 0   MMA issuer (even CTA of a pair only): 4 x tcgen05.mma (K=16) per k-step
 //                   into a TMEM accumulator (two 256-column buffers for the one-CTA form, one
 //                   per pair otherwise); commits release ring stages and hand finished
-//                   accumulators to the epilogues
+//                   accumulators to the epilogues.  The two issuers of a wide pair share
+//                   each token stage; they share the weight stage of a wide tile, while on a
+//                   tall tile each reads, waits for and releases a weight stage of its own
 //   warps 2..5      epilogue: tcgen05.ld, then per mode
 //                     router : fp32 logits [T][E]
 //                     gate/up: rows 0..63 of the CTA's A are gate rows, 64..127 the matching
