@@ -72,3 +72,30 @@ def test_code_digest_ignores_comments_but_not_code(tmp_path, monkeypatch):
     src.write_text("__global__ void k(int* p) {\n  p[0] = 2;\n}\n")
     assert bench.code_digest(["k.cu"]) != a
 
+
+
+def test_clock_summary_keeps_the_timed_region_only():
+    """The clock record summarises only the nvidia-smi samples taken inside the timed region
+    (with 50 ms of slack): idle samples around it, at the maximum clock, do not dilute the
+    clock the timed passes ran at, and the throttle reasons seen inside are listed."""
+    import time as _time
+    base = _time.mktime(_time.strptime("2026/01/02 03:04:05", "%Y/%m/%d %H:%M:%S"))
+
+    def line(dt, mhz, cap):
+        t = base + dt
+        stamp = _time.strftime("%Y/%m/%d %H:%M:%S", _time.localtime(int(t)))
+        stamp += f".{int(round((t - int(t)) * 1000)):03d}"
+        act = "Active" if cap else "Not Active"
+        return (f"{stamp}, 0, {mhz}, 2032, 700.0, 0x0, Not Active, Not Active, Not Active, {act}")
+
+    s = bench.ClockSampler(0)
+    s.lines = [line(0.0, 2032, False), line(0.5, 2032, False),          # idle before
+               line(1.00, 1450, True), line(1.05, 1470, True), line(1.10, 1460, True),
+               line(1.60, 2032, False), line(2.0, 2032, False)]          # idle after
+    out = s.summary(base + 1.0, base + 1.1)
+    assert out["samples"] == 3
+    assert out["sm_mhz"] == 1460.0 and out["sm_max_mhz"] == 2032.0
+    assert out["reasons"] == ["sw_power_cap"] and out["sw_power_cap_samples"] == 3
+    # a region shorter than the sampling period falls back to the nearest samples, and says so
+    out = s.summary(base + 1.3, base + 1.32)
+    assert "note" in out and out["samples"] == 3
