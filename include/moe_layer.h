@@ -272,7 +272,10 @@ int moe_load_expectation(int tokens_per_gpu, int E, int k, int n_gpus, int n_red
                          double* slots_per_gpu, double* tokens_per_expert);
 int moe_load_report(const int* expert_counts, int E, int n_groups, double* report);
 
-/* Kernel launches one moe_layer_forward makes for this shape (for launch accounting). */
+/* Kernel launches one moe_layer_forward makes for this shape (for launch accounting), without
+ * options: group-limited routing and a capacity launch the same kernels; rerouting adds four
+ * launches per round (reroute + 1 rounds), one to set up and one to finish (and a memset of
+ * the dropped-assignment counter when one is given). */
 int moe_layer_num_launches(const moe_shape* s);
 
 /* Reads the device status word of a workspace after the caller's work on it has finished:
